@@ -1,0 +1,174 @@
+/*
+ * drafthead: the reduced-vocabulary draft head of an MTP drafter on one GB300.
+ *
+ * The drafter's lm_head is restricted to a draft vocabulary: the kept rows of
+ * the BF16 target head are gathered (padded to a multiple of 64 rows with
+ * copies of the first kept id), quantised to NVFP4 (or per-tensor FP8), and
+ * each draft step runs a GEMV of BF16 hidden states against that head with
+ * fp32 accumulation, fused with the argmax over kept rows and the map back to
+ * target ids. compute_logits scatters the logits into a full-vocabulary fp32
+ * row prefilled with -inf.
+ *
+ * Sources, by page and section:
+ *   "q38_draft.py" (Qwen3.8-Flash-Next MTP drafter patch): load_draft_model
+ *       (keep mask, dh_idx, pad to N % 64, W[idx] gather, NVFP4 W4A16 head),
+ *       get_top_tokens (dh_idx[draft_head(h).argmax(-1)]), compute_logits.
+ *   "Qwen3.8-Flash-Next-ABLITERATED - MTP drafter, NVFP4 experts + 98K FP8
+ *       head", "How it was built": the NVFP4 recipe (global scale
+ *       amax/(6*448), E4M3 block scales per 16, e2m1 round-to-nearest-even)
+ *       and the 98,304-row E4M3 per-tensor head.
+ *   "FP8 MTP draft stack for vLLM - +6.6% decode on modelopt NVFP4
+ *       Qwen3.5-family checkpoints": _fp8_convert_draft_head (amax clamped
+ *       at 1e-12, scale = amax/448, clamp, cast) and compute_logits
+ *       (new_full(-inf) + index_copy_).
+ *
+ * Conventions for every entry point:
+ *   - Every pointer is a DEVICE pointer unless its name ends in _host.
+ *     The caller allocates and owns all memory, workspaces included; the
+ *     library never allocates, frees or keeps a pointer after a call returns.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream). Calls
+ *     enqueue work and return without synchronising, except
+ *     draft_head_read_device_error, which synchronises `stream`.
+ *   - Arguments are checked on the host before any launch. A failed check
+ *     returns a dh_status and launches nothing. Launch failures return
+ *     DH_ERR_CUDA. Nothing throws across this interface.
+ *   - Faults the host cannot see (a dh_idx entry outside [0, V)) are recorded
+ *     in the workspace's device error word; the offending row is skipped.
+ *     Read them with draft_head_read_device_error.
+ *   - Ids are int32 (V < 2^31); the pages' int64 ids have the same values.
+ *   - One call at a time per workspace: two calls in flight on the GPU that
+ *     share a workspace race on its argmax keys.
+ */
+#ifndef DRAFTHEAD_H
+#define DRAFTHEAD_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define DH_ABI_VERSION 1
+#define DH_MAX_M 16             /* concurrent drafts per call */
+#define DH_WORKSPACE_ALIGN 256  /* required alignment of every workspace */
+
+typedef enum {
+    DH_OK = 0,
+    DH_ERR_ARG = 1,       /* NULL pointer, unknown format, bad count */
+    DH_ERR_SHAPE = 2,     /* shape outside what the kernels support */
+    DH_ERR_ALIGN = 3,     /* pointer not aligned as documented */
+    DH_ERR_WORKSPACE = 4, /* workspace too small or misaligned */
+    DH_ERR_CUDA = 5,      /* a CUDA call or launch failed */
+    DH_ERR_TIMEOUT = 6,   /* reserved: a bounded device wait gave up */
+    DH_ERR_DEVICE = 7     /* the device error word is set (see below) */
+} dh_status;
+
+/* Bits of the device error word. */
+#define DH_DEVERR_IDX 1u  /* a dh_idx entry was outside [0, V) */
+
+typedef enum { DH_FMT_NVFP4 = 1, DH_FMT_FP8 = 2, DH_FMT_BF16 = 3 } dh_format;
+
+/* A quantised draft head. Plain descriptor: the library never owns these.
+ *   fmt     DH_FMT_NVFP4: q = E2M1 codes [N][K/2], element 2i of a row in the
+ *                         low nibble of byte i; sf = E4M3 block scales [N][K/16];
+ *                         scale = &g (global scale, 1 float).
+ *           DH_FMT_FP8:   q = E4M3 codes [N][K] row-major; sf = NULL;
+ *                         scale = &s (per-tensor scale, 1 float).
+ *           DH_FMT_BF16:  q = BF16 weights [N][K] row-major; sf = NULL;
+ *                         scale = NULL (no scaling).
+ *   V       target vocabulary size (width of the compute_logits rows).
+ *   K       hidden size. Supported by the draft-step kernels: 256, 2560
+ *           (the pages' drafter hidden size) and 5120.
+ *   N       head rows, N % 64 == 0 (the pages pad dh_idx so that N % 64 == 0).
+ *   n_kept  rows that are real (1 <= n_kept <= N); rows n_kept..N-1 are the
+ *           padding copies of row 0 and take no part in argmax or scatter.
+ *   idx     dh_idx [N] int32, target id of each row. May be NULL only for a
+ *           BF16 full-vocabulary head (then the row is the id, N == n_kept <= V).
+ * q and sf must be 16-byte aligned. */
+typedef struct dh_head {
+    int fmt;
+    int V;
+    int K;
+    int N;
+    int n_kept;
+    const void *q;
+    const uint8_t *sf;
+    const float *scale;
+    const int32_t *idx;
+} dh_head_t;
+
+/* Build dh_idx on the host ("q38_draft.py", load_draft_model: keep.nonzero(),
+ * pad = (-n) % 64 copies of the first kept id). keep_host: V bytes, non-zero =
+ * kept. Writes *N ids to idx_host (cap entries available), *n_kept and *N.
+ * Errors: DH_ERR_ARG for NULL pointers, V <= 0 or an empty mask (the pages'
+ * idx[:1] would be empty); DH_ERR_SHAPE if cap is too small. */
+int draft_head_build_index(const uint8_t *keep_host, int V, int32_t *idx_host, int cap,
+                           int *n_kept, int *N);
+
+/* Bytes of workspace the quantisers need (a multiple of DH_WORKSPACE_ALIGN). */
+size_t draft_head_quantize_workspace_bytes(void);
+
+/* Gather + NVFP4 quantisation of the rows W[idx[n], :], n < N ("Qwen3.8-Flash-
+ * Next-ABLITERATED ...", "How it was built"; "q38_draft.py", load_draft_model).
+ *   W   BF16 [V][K] row-major target head, 16-byte aligned.
+ *   idx int32 [N], entries in [0, V) (out-of-range rows are skipped and set
+ *       DH_DEVERR_IDX in the workspace's error word).
+ *   q   out [N][K/2] codes; sf out [N][K/16] E4M3 scales; g out: 1 float.
+ *   ws  draft_head_quantize_workspace_bytes() bytes, 256-byte aligned.
+ * g = max(amax, 1e-12) / 2688 in fp32; per block of 16: s = E4M3_RNE_sat(
+ * bamax / fp32(6 g)); codes = E2M1_RNE(clamp(w / fp32(dec(s) g), +-6)) (a
+ * zero scale gives signed zeros). K % 16 == 0, N % 64 == 0. Two kernels on
+ * `stream`, no host synchronisation. */
+int nvfp4_quantize_rows(const void *W, int V, int K, const int32_t *idx, int N,
+                        uint8_t *q, uint8_t *sf, float *g, void *ws, size_t ws_bytes,
+                        void *stream);
+
+/* Gather + per-tensor FP8 E4M3 quantisation of the rows W[idx[n], :]
+ * ("FP8 MTP draft stack ...", _fp8_convert_draft_head): scale =
+ * max(amax, 1e-12) / 448 in fp32, q = E4M3_RNE(clamp(w / scale, +-448)),
+ * stored row-major [N][K] (the page stores the transpose; same bytes).
+ * Arguments as for nvfp4_quantize_rows. */
+int fp8_quantize_rows(const void *W, int V, int K, const int32_t *idx, int N,
+                      uint8_t *q, float *scale, void *ws, size_t ws_bytes, void *stream);
+
+/* Bytes of workspace the draft-step calls need for up to M_max drafts. */
+size_t draft_head_workspace_bytes(const dh_head_t *hd, int M_max);
+
+/* Zero a draft-step workspace (argmax keys, ticket, error word). Call once
+ * after allocating it; every later call leaves it zeroed again. */
+int draft_head_workspace_init(void *ws, size_t ws_bytes, void *stream);
+
+/* get_top_tokens ("q38_draft.py"): for each draft m < M,
+ *   y[m, n] = scale * sum_k w[n, k] * h[m, k]  (fp32 accumulation),
+ *   r*      = the lowest row n < n_kept with the largest y[m, n],
+ *   ids[m]  = idx[r*]  (or r* when idx is NULL),
+ *   top_logit[m] = y[m, r*] if top_logit is not NULL.
+ * h: BF16 [M][K] row-major, 16-byte aligned; ids: int32 [M]; 1 <= M <= 16.
+ * One kernel launch; capturable in a CUDA graph (no allocation, no sync). */
+int draft_head_top_tokens(const dh_head_t *hd, const void *h, int M, int32_t *ids,
+                          float *top_logit, void *ws, size_t ws_bytes, void *stream);
+
+/* compute_logits ("q38_draft.py" compute_logits; "FP8 MTP draft stack ...",
+ * Qwen3_5MTP.compute_logits): out fp32 [M][V] row-major, 16-byte aligned;
+ * out[m, :] = -inf, then out[m, idx[n]] = y[m, n] for n < n_kept. idx entries
+ * of the kept rows must be distinct. Two kernel launches (the -inf fill, then
+ * the GEMV writing its logits in place); capturable in a CUDA graph. */
+int draft_head_compute_logits(const dh_head_t *hd, const void *h, int M, float *out,
+                              void *ws, size_t ws_bytes, void *stream);
+
+/* Synchronise `stream`, then read and clear the device error word of `ws`
+ * (draft-step or quantiser workspace). *err = 0 when nothing was recorded. */
+int draft_head_read_device_error(void *ws, int *err, void *stream);
+
+/* Static description of a status code. */
+const char *draft_head_status_string(int status);
+
+/* DH_ABI_VERSION of the loaded library. */
+int draft_head_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DRAFTHEAD_H */

@@ -1,0 +1,256 @@
+"""Python binding of libdrafthead.so (the reduced-vocabulary NVFP4 draft head).
+
+Argument marshalling only: every step of the path runs in the library's CUDA
+kernels. PyTorch provides device memory and the current stream. If the compiled
+library is missing, every call raises; there is no fallback.
+
+Names follow the C ABI in include/drafthead.h:
+  draft_head_build_index   keep mask -> dh_idx (padded to N % 64 == 0)
+  nvfp4_quantize_rows      gather + NVFP4 quantisation of W[dh_idx]
+  fp8_quantize_rows        gather + per-tensor FP8 E4M3 quantisation
+  DraftHead.top_tokens     get_top_tokens: dh_idx[argmax_n (W_q h)]
+  DraftHead.compute_logits compute_logits: -inf row + logits at dh_idx
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+
+import numpy as np
+import torch
+
+from . import build as _build
+
+DH_OK, DH_ERR_ARG, DH_ERR_SHAPE, DH_ERR_ALIGN, DH_ERR_WORKSPACE, DH_ERR_CUDA = 0, 1, 2, 3, 4, 5
+DH_FMT_NVFP4, DH_FMT_FP8, DH_FMT_BF16 = 1, 2, 3
+DH_MAX_M = 16
+DH_WORKSPACE_ALIGN = 256
+DH_DEVERR_IDX = 1
+
+EXPORTS = (
+    "draft_head_build_index", "draft_head_quantize_workspace_bytes", "nvfp4_quantize_rows",
+    "fp8_quantize_rows", "draft_head_workspace_bytes", "draft_head_workspace_init",
+    "draft_head_top_tokens", "draft_head_compute_logits", "draft_head_read_device_error",
+    "draft_head_status_string", "draft_head_abi_version",
+)
+
+_lib = None
+
+
+class DraftHeadError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        msg = lib().draft_head_status_string(status).decode() if _lib is not None else str(status)
+        super().__init__(f"{fn}: status {status} ({msg})")
+        self.status = status
+
+
+class dh_head_t(C.Structure):
+    _fields_ = [("fmt", C.c_int), ("V", C.c_int), ("K", C.c_int), ("N", C.c_int),
+                ("n_kept", C.c_int), ("q", C.c_void_p), ("sf", C.c_void_p),
+                ("scale", C.c_void_p), ("idx", C.c_void_p)]
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def lib():
+    """Load libdrafthead.so (built by ``nvfp4_draft_head_gb300.build``); raises if absent."""
+    global _lib
+    if _lib is None:
+        path = library_path()
+        if not os.path.exists(path):
+            raise RuntimeError(f"libdrafthead.so is not built ({path}); run "
+                               "`python -m nvfp4_draft_head_gb300.build`")
+        L = C.CDLL(path)
+        P, I, S = C.c_void_p, C.c_int, C.c_size_t
+        L.draft_head_build_index.argtypes = [P, I, P, I, P, P]
+        L.draft_head_quantize_workspace_bytes.argtypes = []
+        L.draft_head_quantize_workspace_bytes.restype = S
+        L.nvfp4_quantize_rows.argtypes = [P, I, I, P, I, P, P, P, P, S, P]
+        L.fp8_quantize_rows.argtypes = [P, I, I, P, I, P, P, P, S, P]
+        L.draft_head_workspace_bytes.argtypes = [C.POINTER(dh_head_t), I]
+        L.draft_head_workspace_bytes.restype = S
+        L.draft_head_workspace_init.argtypes = [P, S, P]
+        L.draft_head_top_tokens.argtypes = [C.POINTER(dh_head_t), P, I, P, P, P, S, P]
+        L.draft_head_compute_logits.argtypes = [C.POINTER(dh_head_t), P, I, P, P, S, P]
+        L.draft_head_read_device_error.argtypes = [P, P, P]
+        L.draft_head_status_string.argtypes = [I]
+        L.draft_head_status_string.restype = C.c_char_p
+        L.draft_head_abi_version.argtypes = []
+        _lib = L
+    return _lib
+
+
+def _check(fn: str, st: int):
+    if st != DH_OK:
+        raise DraftHeadError(fn, st)
+
+
+def _ptr(t) -> int | None:
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream=None) -> int:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return s.cuda_stream
+
+
+def _workspace(nbytes: int, device) -> torch.Tensor:
+    """Zeroed device buffer whose data pointer is DH_WORKSPACE_ALIGN-aligned."""
+    buf = torch.zeros(nbytes + DH_WORKSPACE_ALIGN, dtype=torch.uint8, device=device)
+    off = (-buf.data_ptr()) % DH_WORKSPACE_ALIGN
+    return buf[off: off + nbytes]
+
+
+# ---------------------------------------------------------------- head build --
+
+def draft_head_build_index(keep) -> tuple[np.ndarray, int]:
+    """(dh_idx int32[N], n_kept) from a host keep mask (numpy or CPU tensor)."""
+    keep = np.ascontiguousarray(np.asarray(keep).astype(np.uint8))
+    V = keep.size
+    idx = np.empty(V + 64, dtype=np.int32)
+    nk, N = C.c_int(), C.c_int()
+    _check("draft_head_build_index",
+           lib().draft_head_build_index(keep.ctypes.data, V, idx.ctypes.data, idx.size,
+                                        C.byref(nk), C.byref(N)))
+    return idx[: N.value].copy(), nk.value
+
+
+def _gather_args(W: torch.Tensor, idx: torch.Tensor):
+    if W.dtype != torch.bfloat16 or W.dim() != 2 or not W.is_cuda or not W.is_contiguous():
+        raise ValueError("W must be a contiguous [V, K] bfloat16 CUDA tensor")
+    if idx.dtype != torch.int32 or idx.dim() != 1 or idx.device != W.device:
+        raise ValueError("idx must be an int32 vector on W's device")
+    return W.shape[0], W.shape[1], idx.numel()
+
+
+def nvfp4_quantize_rows(W: torch.Tensor, idx: torch.Tensor, stream=None):
+    """(q uint8[N, K/2], sf uint8[N, K/16], g float32[1]) of the rows W[idx]."""
+    V, K, N = _gather_args(W, idx)
+    q = torch.empty((N, K // 2), dtype=torch.uint8, device=W.device)
+    sf = torch.empty((N, K // 16), dtype=torch.uint8, device=W.device)
+    g = torch.empty(1, dtype=torch.float32, device=W.device)
+    nb = lib().draft_head_quantize_workspace_bytes()
+    ws = _workspace(nb, W.device)
+    _check("nvfp4_quantize_rows",
+           lib().nvfp4_quantize_rows(W.data_ptr(), V, K, idx.data_ptr(), N, q.data_ptr(),
+                                     sf.data_ptr(), g.data_ptr(), ws.data_ptr(), nb, _stream(stream)))
+    _raise_device_error(ws, stream, "nvfp4_quantize_rows")
+    return q, sf, g
+
+
+def fp8_quantize_rows(W: torch.Tensor, idx: torch.Tensor, stream=None):
+    """(q uint8[N, K] E4M3 codes, scale float32[1]) of the rows W[idx]."""
+    V, K, N = _gather_args(W, idx)
+    q = torch.empty((N, K), dtype=torch.uint8, device=W.device)
+    s = torch.empty(1, dtype=torch.float32, device=W.device)
+    nb = lib().draft_head_quantize_workspace_bytes()
+    ws = _workspace(nb, W.device)
+    _check("fp8_quantize_rows",
+           lib().fp8_quantize_rows(W.data_ptr(), V, K, idx.data_ptr(), N, q.data_ptr(),
+                                   s.data_ptr(), ws.data_ptr(), nb, _stream(stream)))
+    _raise_device_error(ws, stream, "fp8_quantize_rows")
+    return q, s
+
+
+def draft_head_read_device_error(ws: torch.Tensor, stream=None) -> int:
+    err = C.c_int()
+    _check("draft_head_read_device_error",
+           lib().draft_head_read_device_error(ws.data_ptr(), C.byref(err), _stream(stream)))
+    return err.value
+
+
+def _raise_device_error(ws, stream, fn):
+    err = draft_head_read_device_error(ws, stream)
+    if err:
+        raise RuntimeError(f"{fn}: device error word {err:#x} (a dh_idx entry outside [0, V))")
+
+
+# ---------------------------------------------------------------- draft step --
+
+class DraftHead:
+    """A quantised draft head plus its workspace; tensors stay owned by torch.
+
+    fmt: DH_FMT_NVFP4 (q, sf, scale=g), DH_FMT_FP8 (q, scale) or DH_FMT_BF16 (q =
+    the BF16 weights, idx may be None for a full-vocabulary head).
+    """
+
+    def __init__(self, fmt: int, V: int, q: torch.Tensor, idx: torch.Tensor | None, n_kept: int,
+                 sf: torch.Tensor | None = None, scale: torch.Tensor | None = None):
+        self.fmt, self.V, self.n_kept = fmt, int(V), int(n_kept)
+        self.q, self.sf, self.scale, self.idx = q, sf, scale, idx
+        self.N = q.shape[0]
+        if fmt == DH_FMT_NVFP4:
+            self.K = q.shape[1] * 2
+        elif fmt == DH_FMT_FP8:
+            self.K = q.shape[1]
+        else:
+            self.K = q.shape[1] if q.dtype == torch.bfloat16 else q.shape[1] // 2
+        self.desc = dh_head_t(fmt, self.V, self.K, self.N, self.n_kept, _ptr(q), _ptr(sf),
+                              _ptr(scale), _ptr(idx))
+        self.ws_bytes = lib().draft_head_workspace_bytes(C.byref(self.desc), DH_MAX_M)
+        self.ws = _workspace(self.ws_bytes, q.device)
+        _check("draft_head_workspace_init",
+               lib().draft_head_workspace_init(self.ws.data_ptr(), self.ws_bytes, _stream()))
+
+    def with_storage(self, q: torch.Tensor, sf: torch.Tensor | None = None) -> "DraftHead":
+        """The same head (same scale, idx, workspace) read from another copy of q / sf."""
+        other = object.__new__(DraftHead)
+        other.__dict__.update(self.__dict__)
+        other.q, other.sf = q, (sf if sf is not None else self.sf)
+        other.desc = dh_head_t(self.fmt, self.V, self.K, self.N, self.n_kept, _ptr(other.q),
+                               _ptr(other.sf), _ptr(self.scale), _ptr(self.idx))
+        return other
+
+    def top_tokens(self, h: torch.Tensor, ids: torch.Tensor | None = None,
+                   top: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+        """get_top_tokens: int32[M] target ids of the argmax over kept rows."""
+        M = self._check_h(h)
+        if ids is None:
+            ids = torch.empty(M, dtype=torch.int32, device=h.device)
+        _check("draft_head_top_tokens",
+               lib().draft_head_top_tokens(C.byref(self.desc), h.data_ptr(), M, ids.data_ptr(),
+                                           _ptr(top), self.ws.data_ptr(), self.ws_bytes,
+                                           _stream(stream)))
+        return ids
+
+    def compute_logits(self, h: torch.Tensor, out: torch.Tensor | None = None,
+                       stream=None) -> torch.Tensor:
+        """compute_logits: float32[M, V], -inf outside the kept ids."""
+        M = self._check_h(h)
+        if out is None:
+            out = torch.empty((M, self.V), dtype=torch.float32, device=h.device)
+        _check("draft_head_compute_logits",
+               lib().draft_head_compute_logits(C.byref(self.desc), h.data_ptr(), M, out.data_ptr(),
+                                               self.ws.data_ptr(), self.ws_bytes, _stream(stream)))
+        return out
+
+    def device_error(self, stream=None) -> int:
+        return draft_head_read_device_error(self.ws, stream)
+
+    def _check_h(self, h: torch.Tensor) -> int:
+        if h.dtype != torch.bfloat16 or h.dim() != 2 or h.shape[1] != self.K or not h.is_contiguous():
+            raise ValueError(f"h must be a contiguous [M, {self.K}] bfloat16 tensor")
+        return h.shape[0]
+
+
+def nvfp4_head(W: torch.Tensor, keep, stream=None) -> DraftHead:
+    """Build an NVFP4 draft head from a BF16 target head and a host keep mask."""
+    idx_np, nk = draft_head_build_index(keep)
+    idx = torch.from_numpy(idx_np).to(W.device)
+    q, sf, g = nvfp4_quantize_rows(W, idx, stream)
+    return DraftHead(DH_FMT_NVFP4, W.shape[0], q, idx, nk, sf=sf, scale=g)
+
+
+def fp8_head(W: torch.Tensor, keep, stream=None) -> DraftHead:
+    """Build a per-tensor FP8 draft head from a BF16 target head and a host keep mask."""
+    idx_np, nk = draft_head_build_index(keep)
+    idx = torch.from_numpy(idx_np).to(W.device)
+    q, s = fp8_quantize_rows(W, idx, stream)
+    return DraftHead(DH_FMT_FP8, W.shape[0], q, idx, nk, scale=s)
+
+
+def bf16_full_head(W: torch.Tensor) -> DraftHead:
+    """The stock full-vocabulary BF16 head (the row is the id)."""
+    return DraftHead(DH_FMT_BF16, W.shape[0], W, None, W.shape[0])

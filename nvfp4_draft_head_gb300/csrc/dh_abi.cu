@@ -1,0 +1,194 @@
+// C-ABI front end of libdrafthead.so: argument checks on the host, then the
+// kernel launches of dh_quantize.cu and dh_gemv*.cu. See include/drafthead.h.
+#include <cstdint>
+#include <cstring>
+#include <cuda_runtime.h>
+
+#include "../../include/drafthead.h"
+#include "dh_common.cuh"
+#include "dh_internal.h"
+
+namespace {
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? DH_OK : DH_ERR_CUDA; }
+
+int check_ws(const void* ws, size_t ws_bytes, size_t need) {
+    if (ws == nullptr) return DH_ERR_ARG;
+    if (!aligned(ws, DH_WORKSPACE_ALIGN) || ws_bytes < need) return DH_ERR_WORKSPACE;
+    return DH_OK;
+}
+
+int check_gather(const void* W, int V, int K, const int32_t* idx, int N) {
+    if (W == nullptr || idx == nullptr) return DH_ERR_ARG;
+    if (V <= 0 || K <= 0 || N <= 0) return DH_ERR_SHAPE;
+    if (K % 16 != 0 || N % 64 != 0) return DH_ERR_SHAPE;
+    if (static_cast<long long>(N) * K >= (1ll << 40)) return DH_ERR_SHAPE;
+    if (!aligned(W, 16) || !aligned(idx, 4)) return DH_ERR_ALIGN;
+    return DH_OK;
+}
+
+int check_head(const dh_head_t* hd) {
+    if (hd == nullptr || hd->q == nullptr) return DH_ERR_ARG;
+    if (hd->fmt != DH_FMT_NVFP4 && hd->fmt != DH_FMT_FP8 && hd->fmt != DH_FMT_BF16) return DH_ERR_ARG;
+    if (hd->V <= 0 || hd->N <= 0 || hd->n_kept < 1 || hd->n_kept > hd->N) return DH_ERR_SHAPE;
+    if (hd->N % 64 != 0) return DH_ERR_SHAPE;
+    if (!dh::gemv_supported(hd->fmt, hd->K)) return DH_ERR_SHAPE;
+    if (hd->fmt == DH_FMT_NVFP4 && (hd->sf == nullptr || hd->scale == nullptr)) return DH_ERR_ARG;
+    if (hd->fmt == DH_FMT_FP8 && hd->scale == nullptr) return DH_ERR_ARG;
+    if (hd->idx == nullptr) {
+        if (hd->fmt != DH_FMT_BF16) return DH_ERR_ARG;
+        if (hd->n_kept != hd->N || hd->N > hd->V) return DH_ERR_SHAPE;
+    }
+    if (!aligned(hd->q, 16) || (hd->sf && !aligned(hd->sf, 16))) return DH_ERR_ALIGN;
+    if ((hd->scale && !aligned(hd->scale, 4)) || (hd->idx && !aligned(hd->idx, 4))) return DH_ERR_ALIGN;
+    return DH_OK;
+}
+
+int check_step(const dh_head_t* hd, const void* h, int M) {
+    int st = check_head(hd);
+    if (st != DH_OK) return st;
+    if (h == nullptr) return DH_ERR_ARG;
+    if (M < 1 || M > DH_MAX_M) return DH_ERR_SHAPE;
+    if (!aligned(h, 16)) return DH_ERR_ALIGN;
+    return DH_OK;
+}
+
+dh::GemvArgs make_args(const dh_head_t* hd, const void* h, int M, void* ws) {
+    dh::GemvArgs a;
+    std::memset(&a, 0, sizeof a);
+    a.fmt = hd->fmt;
+    a.K = hd->K;
+    a.V = hd->V;
+    a.N = hd->N;
+    a.n_kept = hd->n_kept;
+    a.q = hd->q;
+    a.sf = hd->sf;
+    a.scale = hd->scale;
+    a.idx = hd->idx;
+    a.h = static_cast<const uint16_t*>(h);
+    a.M = M;
+    a.ws = static_cast<dh::Workspace*>(ws);
+    return a;
+}
+
+}  // namespace
+
+extern "C" {
+
+int draft_head_abi_version(void) { return DH_ABI_VERSION; }
+
+const char* draft_head_status_string(int status) {
+    switch (status) {
+        case DH_OK: return "ok";
+        case DH_ERR_ARG: return "invalid argument (NULL pointer, unknown format or count)";
+        case DH_ERR_SHAPE: return "unsupported shape";
+        case DH_ERR_ALIGN: return "pointer not aligned as documented";
+        case DH_ERR_WORKSPACE: return "workspace too small or misaligned";
+        case DH_ERR_CUDA: return "CUDA call or kernel launch failed";
+        case DH_ERR_TIMEOUT: return "bounded device wait timed out";
+        case DH_ERR_DEVICE: return "device error word set";
+        default: return "unknown status";
+    }
+}
+
+int draft_head_build_index(const uint8_t* keep_host, int V, int32_t* idx_host, int cap, int* n_kept,
+                           int* N) {
+    if (keep_host == nullptr || idx_host == nullptr || n_kept == nullptr || N == nullptr) return DH_ERR_ARG;
+    if (V <= 0 || cap < 0) return DH_ERR_ARG;
+    int n = 0;
+    for (int v = 0; v < V; ++v) {
+        if (!keep_host[v]) continue;
+        if (n >= cap) return DH_ERR_SHAPE;
+        idx_host[n++] = v;
+    }
+    if (n == 0) return DH_ERR_ARG;
+    const int pad = (64 - n % 64) % 64;
+    if (n + pad > cap) return DH_ERR_SHAPE;
+    for (int i = 0; i < pad; ++i) idx_host[n + i] = idx_host[0];
+    *n_kept = n;
+    *N = n + pad;
+    return DH_OK;
+}
+
+size_t draft_head_quantize_workspace_bytes(void) { return sizeof(dh::Workspace); }
+
+int nvfp4_quantize_rows(const void* W, int V, int K, const int32_t* idx, int N, uint8_t* q,
+                        uint8_t* sf, float* g, void* ws, size_t ws_bytes, void* stream) {
+    int st = check_gather(W, V, K, idx, N);
+    if (st != DH_OK) return st;
+    if (q == nullptr || sf == nullptr || g == nullptr) return DH_ERR_ARG;
+    if (!aligned(q, 16) || !aligned(sf, 16) || !aligned(g, 4)) return DH_ERR_ALIGN;
+    if ((st = check_ws(ws, ws_bytes, sizeof(dh::Workspace))) != DH_OK) return st;
+    return cuda_status(dh::launch_nvfp4_quantize(static_cast<const uint16_t*>(W), V, K, idx, N, q, sf,
+                                                 g, static_cast<dh::Workspace*>(ws),
+                                                 static_cast<cudaStream_t>(stream)));
+}
+
+int fp8_quantize_rows(const void* W, int V, int K, const int32_t* idx, int N, uint8_t* q,
+                      float* scale, void* ws, size_t ws_bytes, void* stream) {
+    int st = check_gather(W, V, K, idx, N);
+    if (st != DH_OK) return st;
+    if (q == nullptr || scale == nullptr) return DH_ERR_ARG;
+    if (!aligned(q, 16) || !aligned(scale, 4)) return DH_ERR_ALIGN;
+    if ((st = check_ws(ws, ws_bytes, sizeof(dh::Workspace))) != DH_OK) return st;
+    return cuda_status(dh::launch_fp8_quantize(static_cast<const uint16_t*>(W), V, K, idx, N, q, scale,
+                                               static_cast<dh::Workspace*>(ws),
+                                               static_cast<cudaStream_t>(stream)));
+}
+
+size_t draft_head_workspace_bytes(const dh_head_t* hd, int M_max) {
+    (void)hd;
+    (void)M_max;
+    return sizeof(dh::Workspace);
+}
+
+int draft_head_workspace_init(void* ws, size_t ws_bytes, void* stream) {
+    int st = check_ws(ws, ws_bytes, sizeof(dh::Workspace));
+    if (st != DH_OK) return st;
+    return cuda_status(cudaMemsetAsync(ws, 0, sizeof(dh::Workspace), static_cast<cudaStream_t>(stream)));
+}
+
+int draft_head_top_tokens(const dh_head_t* hd, const void* h, int M, int32_t* ids, float* top_logit,
+                          void* ws, size_t ws_bytes, void* stream) {
+    int st = check_step(hd, h, M);
+    if (st != DH_OK) return st;
+    if (ids == nullptr) return DH_ERR_ARG;
+    if (!aligned(ids, 4) || (top_logit && !aligned(top_logit, 4))) return DH_ERR_ALIGN;
+    if ((st = check_ws(ws, ws_bytes, sizeof(dh::Workspace))) != DH_OK) return st;
+    dh::GemvArgs a = make_args(hd, h, M, ws);
+    a.ids = ids;
+    a.top = top_logit;
+    return cuda_status(dh::launch_gemv(a, static_cast<cudaStream_t>(stream)));
+}
+
+int draft_head_compute_logits(const dh_head_t* hd, const void* h, int M, float* out, void* ws,
+                              size_t ws_bytes, void* stream) {
+    int st = check_step(hd, h, M);
+    if (st != DH_OK) return st;
+    if (out == nullptr) return DH_ERR_ARG;
+    if (!aligned(out, 16)) return DH_ERR_ALIGN;
+    if ((st = check_ws(ws, ws_bytes, sizeof(dh::Workspace))) != DH_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = dh::launch_fill_neg_inf(out, static_cast<size_t>(M) * hd->V, s);
+    if (e != cudaSuccess) return DH_ERR_CUDA;
+    dh::GemvArgs a = make_args(hd, h, M, ws);
+    a.out = out;
+    return cuda_status(dh::launch_gemv(a, s));
+}
+
+int draft_head_read_device_error(void* ws, int* err, void* stream) {
+    if (ws == nullptr || err == nullptr) return DH_ERR_ARG;
+    if (!aligned(ws, DH_WORKSPACE_ALIGN)) return DH_ERR_WORKSPACE;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    dh::Workspace* w = static_cast<dh::Workspace*>(ws);
+    unsigned int v = 0;
+    if (cudaMemcpyAsync(&v, &w->error, sizeof v, cudaMemcpyDeviceToHost, s) != cudaSuccess) return DH_ERR_CUDA;
+    if (cudaMemsetAsync(&w->error, 0, sizeof v, s) != cudaSuccess) return DH_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return DH_ERR_CUDA;
+    *err = static_cast<int>(v);
+    return DH_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,119 @@
+// Device helpers shared by the draft-head kernels (CUDA side only).
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+#include <cuda_fp16.h>
+
+namespace dh {
+
+// Layout of a draft-step workspace (first 256 bytes; callers allocate it).
+struct Workspace {
+    unsigned long long keys[16];  // per draft: max over rows of (ordered logit << 32 | ~row)
+    unsigned int ticket;          // CTAs that have published their keys this launch
+    unsigned int error;           // DH_DEVERR_* bits
+    unsigned int amax_bits;       // quantisers: running max |w| as float bits
+    unsigned int pad_[29];
+};
+static_assert(sizeof(Workspace) == 256, "workspace header is 256 bytes");
+
+constexpr unsigned int kDevErrIdx = 1u;
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// Order-preserving map of a float to uint32: a < b  <=>  ord(a) < ord(b).
+// -0 is folded onto +0 and every NaN onto the largest key, so that, like
+// torch.argmax, a NaN wins and equal values tie.
+__device__ __forceinline__ uint32_t ordered_key(float v) {
+    uint32_t u = __float_as_uint(v);
+    if (v != v) return 0xFFFFFFFFu;
+    if (v == 0.0f) u = 0u;
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+__device__ __forceinline__ float ordered_value(uint32_t k) {
+    if (k == 0xFFFFFFFFu) return __uint_as_float(0x7FC00000u);
+    uint32_t u = (k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k;
+    return __uint_as_float(u);
+}
+
+// 64-bit argmax key: larger logit first, then the lower row.
+__device__ __forceinline__ unsigned long long argmax_key(uint32_t ord, uint32_t row) {
+    return (static_cast<unsigned long long>(ord) << 32) | (0xFFFFFFFFu - row);
+}
+
+// Streaming 16-byte load that does not allocate in L1 (the head is read once).
+__device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
+    uint4 r;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t ld_stream_u16(const void* p) {
+    unsigned short r;
+    asm volatile("ld.global.nc.L1::no_allocate.u16 %0, [%1];" : "=h"(r) : "l"(p));
+    return r;
+}
+
+// Four E2M1 pairs (one 32-bit word, 8 codes) to four f16x2: byte i -> out[i],
+// low nibble -> low half. Exact: every E2M1 value is an f16.
+__device__ __forceinline__ void e2m1x8_to_f16x2(uint32_t w, uint32_t (&o)[4]) {
+    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+        "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %2, b2;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+        : "=r"(o[0]), "=r"(o[1]), "=r"(o[2]), "=r"(o[3]) : "r"(w));
+}
+
+// Two E4M3 bytes (low 16 bits of w) to f16x2, low byte -> low half. Exact.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t w) {
+    uint32_t r;
+    asm("{\n\t.reg .b16 t;\n\tcvt.u16.u32 t, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, t;\n\t}"
+        : "=r"(r) : "r"(w));
+    return r;
+}
+
+__device__ __forceinline__ float f16lo(uint32_t x) { return __half2float(__ushort_as_half((unsigned short)(x & 0xFFFFu))); }
+__device__ __forceinline__ float f16hi(uint32_t x) { return __half2float(__ushort_as_half((unsigned short)(x >> 16))); }
+
+// acc += a.lo * b.lo + a.hi * b.hi with f16 operands and an fp32 accumulator
+// (each product is exact in fp32; two roundings of the running sum).
+__device__ __forceinline__ float fma2_f16_f32(uint32_t a, uint32_t b, float acc) {
+    asm("{\n\t.reg .f16 a0, a1, b0, b1;\n\t"
+        "mov.b32 {a0, a1}, %1;\n\tmov.b32 {b0, b1}, %2;\n\t"
+        "fma.rn.f32.f16 %0, a0, b0, %0;\n\tfma.rn.f32.f16 %0, a1, b1, %0;\n\t}"
+        : "+f"(acc) : "r"(a), "r"(b));
+    return acc;
+}
+
+// Same with BF16 operands.
+__device__ __forceinline__ float fma2_bf16_f32(uint32_t a, uint32_t b, float acc) {
+    asm("{\n\t.reg .b16 a0, a1, b0, b1;\n\t"
+        "mov.b32 {a0, a1}, %1;\n\tmov.b32 {b0, b1}, %2;\n\t"
+        "fma.rn.f32.bf16 %0, a0, b0, %0;\n\tfma.rn.f32.bf16 %0, a1, b1, %0;\n\t}"
+        : "+f"(acc) : "r"(a), "r"(b));
+    return acc;
+}
+
+// Power of two 2^e with e clamped to the normal float range.
+__device__ __forceinline__ float exp2i(int e) {
+    e = e < -126 ? -126 : (e > 127 ? 127 : e);
+    return __uint_as_float(static_cast<uint32_t>(e + 127) << 23);
+}
+
+// Exponent e such that amax * 2^e lies in [2^14, 2^15): the largest |h| then
+// sits just under the f16 maximum and every BF16 value at most 2^24 times
+// smaller converts to f16 exactly (BF16 has 8 significant bits, f16 11).
+__device__ __forceinline__ int f16_prescale_exponent(float amax) {
+    if (!(amax > 0.0f)) return 0;
+    // floor(log2 amax) for a normal amax; a subnormal amax reads as -127 and
+    // the resulting large exponent is clamped by exp2i.
+    const int E = static_cast<int>((__float_as_uint(amax) >> 23) & 0xFF) - 127;
+    return 14 - E;
+}
+
+}  // namespace dh

@@ -1,0 +1,63 @@
+// Draft-step dispatch: format and hidden size -> kernel instantiation (one
+// translation unit per head format, see dh_gemv_impl.cuh), plus the -inf fill
+// of compute_logits.
+#include "dh_common.cuh"
+#include "dh_internal.h"
+
+namespace dh {
+
+cudaError_t launch_gemv_nvfp4(const GemvArgs& a, cudaStream_t s);
+cudaError_t launch_gemv_fp8(const GemvArgs& a, cudaStream_t s);
+cudaError_t launch_gemv_bf16(const GemvArgs& a, cudaStream_t s);
+
+__global__ void fill_neg_inf_kernel(float4* out4, size_t n4, float* tail, int ntail) {
+    const float ninf = __uint_as_float(0xFF800000u);
+    const float4 v = make_float4(ninf, ninf, ninf, ninf);
+    for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n4;
+         i += static_cast<size_t>(gridDim.x) * blockDim.x)
+        out4[i] = v;
+    if (blockIdx.x == 0 && threadIdx.x < ntail) tail[threadIdx.x] = ninf;
+}
+
+
+int sm_count() {
+    static int cached[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 0;
+    if (dev < 64 && cached[dev] > 0) return cached[dev];
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    if (dev < 64) cached[dev] = n;
+    return n;
+}
+
+#define DH_GEMV_KS(X) X(256) X(2560) X(5120)
+
+bool gemv_supported(int fmt, int K) {
+    if (fmt < 1 || fmt > 3) return false;
+#define DH_CASE(k) if (K == k) return true;
+    DH_GEMV_KS(DH_CASE)
+#undef DH_CASE
+    return false;
+}
+
+cudaError_t launch_gemv(const GemvArgs& a, cudaStream_t s) {
+    if (!gemv_supported(a.fmt, a.K)) return cudaErrorInvalidValue;
+    if (a.fmt == 1) return launch_gemv_nvfp4(a, s);
+    if (a.fmt == 2) return launch_gemv_fp8(a, s);
+    return launch_gemv_bf16(a, s);
+}
+
+cudaError_t launch_fill_neg_inf(float* out, size_t count, cudaStream_t s) {
+    const size_t n4 = count / 4;
+    const int ntail = static_cast<int>(count - n4 * 4);
+    const int sms = sm_count();
+    if (sms <= 0) return cudaErrorInvalidDevice;
+    size_t want = (n4 + 255) / 256;
+    int blocks = static_cast<int>(want < static_cast<size_t>(sms) * 4 ? want : static_cast<size_t>(sms) * 4);
+    if (blocks < 1) blocks = 1;
+    fill_neg_inf_kernel<<<blocks, 256, 0, s>>>(reinterpret_cast<float4*>(out), n4, out + n4 * 4, ntail);
+    return cudaGetLastError();
+}
+
+}  // namespace dh

@@ -1,0 +1,51 @@
+// Internal interface between the C-ABI front end and the kernel files.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace dh {
+
+struct Workspace;
+
+struct GemvArgs {
+    int fmt;
+    int K;
+    int V;
+    int N;
+    int n_kept;
+    const void* q;
+    const uint8_t* sf;
+    const float* scale;
+    const int32_t* idx;
+    const uint16_t* h;   // BF16 [M][K]
+    int M;
+    int32_t* ids;        // top-tokens mode
+    float* top;          // optional
+    float* out;          // logits mode: fp32 [M][V]
+    Workspace* ws;
+};
+
+// True if the draft-step kernels are compiled for (fmt, K).
+bool gemv_supported(int fmt, int K);
+
+// Enqueue the GEMV + argmax (out == nullptr) or GEMV + logits scatter
+// (out != nullptr; the -inf fill must already be enqueued). Returns a
+// cudaError_t of the launch.
+cudaError_t launch_gemv(const GemvArgs& a, cudaStream_t s);
+
+// Fill out[0..count) with -inf.
+cudaError_t launch_fill_neg_inf(float* out, size_t count, cudaStream_t s);
+
+// Quantisers: amax pass + encode pass (ws->amax_bits is cleared first).
+cudaError_t launch_nvfp4_quantize(const uint16_t* W, int V, int K, const int32_t* idx, int N,
+                                  uint8_t* q, uint8_t* sf, float* g, Workspace* ws,
+                                  cudaStream_t s);
+cudaError_t launch_fp8_quantize(const uint16_t* W, int V, int K, const int32_t* idx, int N,
+                                uint8_t* q, float* scale, Workspace* ws, cudaStream_t s);
+
+// Number of SMs of the current device (cached per device).
+int sm_count();
+
+}  // namespace dh

@@ -272,41 +272,53 @@ int or_fp8_quantize(const uint16_t *W, int V, int K, const int32_t *idx, int N,
 /* Draft step: GEMV, argmax, id map, logits scatter                         */
 /* ------------------------------------------------------------------------ */
 
-/* Dequantised weight w'[n, k] of each head format, in fp64 (exact). */
-static double w_nvfp4(const uint8_t *q, const uint8_t *sf, double g, int K, int n, int k)
-{
-    int byte = q[(size_t)n * (K / 2) + k / 2];
-    int code = (k & 1) ? (byte >> 4) : (byte & 15);
-    return or_e2m1_decode(code) * or_e4m3_decode(sf[(size_t)n * (K / 16) + k / 16]) * g;
-}
-
 /* y[m, n] = sum_k w'[n, k] * h[m, k] in fp64, and A[m, n] = sum_k |w'[n, k] h[m, k]|
  * (the scale of the logits tolerance) [Q38 get_top_tokens / compute_logits:
  * draft_head(h)]. fmt: 1 = NVFP4 (q, sf, scale = g), 2 = FP8 (q, scale),
- * 3 = BF16 (q holds the BF16 head, scale unused). Rows are those of the
- * head as stored (N of them). y and A are [M][N]; A may be NULL. */
+ * 3 = BF16 (q holds the BF16 head, scale unused). Each head row is first
+ * dequantised into w'[0..K) (exact in fp64), then dotted with every h row.
+ * Rows are those of the head as stored (N of them). y and A are [M][N];
+ * A may be NULL. */
 int or_gemv(int fmt, const uint8_t *q, const uint8_t *sf, float scale, int N, int K,
             const uint16_t *h, int M, double *y, double *A)
 {
+    double e2[16], e4[256], *w, *hv;
     int m, n, k;
     if (!q || !h || !y || N <= 0 || K <= 0 || M <= 0 || K % 16 != 0)
         return OR_ERR_ARG;
-    if (fmt == 1 && !sf)
+    if ((fmt == 1 && !sf) || fmt < 1 || fmt > 3)
         return OR_ERR_ARG;
-    if (fmt < 1 || fmt > 3)
+    for (k = 0; k < 16; k++)
+        e2[k] = or_e2m1_decode(k);
+    for (k = 0; k < 256; k++)
+        e4[k] = or_e4m3_decode(k);
+    w = (double *)malloc(sizeof(double) * (size_t)K);
+    hv = (double *)malloc(sizeof(double) * (size_t)K * (size_t)M);
+    if (!w || !hv) {
+        free(w);
+        free(hv);
         return OR_ERR_ARG;
+    }
     for (m = 0; m < M; m++)
-        for (n = 0; n < N; n++) {
+        for (k = 0; k < K; k++)
+            hv[(size_t)m * K + k] = bf16_value(h[(size_t)m * K + k]);
+    for (n = 0; n < N; n++) {
+        for (k = 0; k < K; k++) {
+            if (fmt == 1) {
+                int byte = q[(size_t)n * (K / 2) + k / 2];
+                int code = (k & 1) ? (byte >> 4) : (byte & 15);
+                w[k] = e2[code] * e4[sf[(size_t)n * (K / 16) + k / 16]] * (double)scale;
+            } else if (fmt == 2) {
+                w[k] = e4[q[(size_t)n * K + k]] * (double)scale;
+            } else {
+                w[k] = bf16_value(((const uint16_t *)q)[(size_t)n * K + k]);
+            }
+        }
+        for (m = 0; m < M; m++) {
+            const double *x = hv + (size_t)m * K;
             double s = 0.0, a = 0.0;
             for (k = 0; k < K; k++) {
-                double w, p;
-                if (fmt == 1)
-                    w = w_nvfp4(q, sf, scale, K, n, k);
-                else if (fmt == 2)
-                    w = or_e4m3_decode(q[(size_t)n * K + k]) * (double)scale;
-                else
-                    w = bf16_value(((const uint16_t *)q)[(size_t)n * K + k]);
-                p = w * (double)bf16_value(h[(size_t)m * K + k]);
+                double p = w[k] * x[k];
                 s += p;
                 a += fabs(p);
             }
@@ -314,6 +326,9 @@ int or_gemv(int fmt, const uint8_t *q, const uint8_t *sf, float scale, int N, in
             if (A)
                 A[(size_t)m * N + n] = a;
         }
+    }
+    free(w);
+    free(hv);
     return OR_OK;
 }
 

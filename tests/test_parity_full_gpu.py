@@ -1,0 +1,108 @@
+"""Parity at the pages' full sizes (V = 248,320, K = 2560), GPU vs oracle:
+  * the 64,064-row NVFP4 head: gather + quantise bit-exact, draft steps at
+    M = 1 (fresh hidden states, the launch configuration the benchmark times);
+  * the batch sweep M in {1, 2, 4, 8, 16} with planted near-ties (top-2 oracle
+    gap < 1e-3 in 5 % of rows), both get_top_tokens and compute_logits;
+  * the 98,304-row FP8 head: quantise bit-exact, M = 1 and 4, both paths;
+  * the full-vocabulary BF16 head (the stock drafter read) at M = 1.
+The oracle computes every output here (its fp64 GEMV over a whole head takes
+about a second per draft row on one core)."""
+import numpy as np
+import pytest
+import torch
+
+import nvfp4_draft_head_gb300 as dh
+import oracle
+import synthetic as syn
+from parity_util import Workload, check_argmax_rows, check_logits, ids_to_rows, plant_near_ties
+from test_parity_gpu import dev, dev_bf16, run_step
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    from nvfp4_draft_head_gb300 import build
+    build.build()
+
+
+@pytest.fixture(scope="module")
+def W_full():
+    c = syn.QWEN_64K
+    return syn.head_bf16(syn.SEED_HEAD_QWEN, c["V"], c["K"])
+
+
+@pytest.fixture(scope="module")
+def W_dev(W_full):
+    return dev_bf16(W_full)
+
+
+@pytest.fixture(scope="module")
+def qwen64k(W_full):
+    c = syn.QWEN_64K
+    return Workload(syn.SEED_HEAD_QWEN, c["V"], c["K"], c["n_kept"], c["forced"], syn.SEED_KEEP_64K, W=W_full)
+
+
+@pytest.fixture(scope="module")
+def head64k(qwen64k, W_dev):
+    idx = dev(qwen64k.idx)
+    q, sf, g = dh.nvfp4_quantize_rows(W_dev, idx)
+    return dh.DraftHead(dh.DH_FMT_NVFP4, qwen64k.V, q, idx, qwen64k.n_kept, sf=sf, scale=g)
+
+
+def test_qwen64k_index_and_quantize_bit_exact(qwen64k, head64k):
+    assert (qwen64k.n_kept, qwen64k.N) == (64_026, 64_064)
+    q_o, sf_o, g_o = qwen64k.nvfp4()
+    assert np.array_equal(head64k.q.cpu().numpy(), q_o)
+    assert np.array_equal(head64k.sf.cpu().numpy(), sf_o)
+    assert head64k.scale.cpu().numpy()[0] == g_o
+    idx_abi, nk = dh.draft_head_build_index(qwen64k.keep)
+    assert nk == qwen64k.n_kept and np.array_equal(idx_abi, qwen64k.idx)
+
+
+def test_qwen64k_m1_steps(qwen64k, head64k):
+    q_o, sf_o, g_o = qwen64k.nvfp4()
+    for step in range(6):
+        h = syn.hidden_bf16(syn.hidden_seed(1, step), 1, qwen64k.K)
+        run_step(head64k, h, oracle.FMT_NVFP4, q_o, sf_o, g_o, qwen64k.idx, qwen64k.n_kept, qwen64k.V,
+                 f"qwen64k M=1 step {step}")
+
+
+@pytest.mark.parametrize("M", [1, 2, 4, 8, 16])
+def test_batch_sweep_with_near_ties(qwen64k, head64k, M):
+    q_o, sf_o, g_o = qwen64k.nvfp4()
+    steps = 2 if M >= 8 else 4
+    planted_total = 0
+    for step in range(steps):
+        h = syn.hidden_bf16(syn.hidden_seed(3, 1000 * M + step), M, qwen64k.K)
+        if step == 0:
+            h, planted, gaps = plant_near_ties(q_o, sf_o, g_o, h, qwen64k.n_kept, 0.05, seed=M)
+            planted_total += len(planted)
+            assert all(gp < 1e-3 for gp in gaps)
+        run_step(head64k, h, oracle.FMT_NVFP4, q_o, sf_o, g_o, qwen64k.idx, qwen64k.n_kept, qwen64k.V,
+                 f"sweep M={M} step {step}")
+    assert planted_total >= 1
+
+
+def test_fp8_98k_head(W_full, W_dev):
+    c = syn.FP8_98K
+    wl = Workload(syn.SEED_HEAD_QWEN, c["V"], c["K"], c["n_kept"], c["forced"], syn.SEED_KEEP_98K, W=W_full)
+    assert wl.N == 98_304
+    idx = dev(wl.idx)
+    q, s = dh.fp8_quantize_rows(W_dev, idx)
+    q_o, s_o = wl.fp8()
+    assert np.array_equal(q.cpu().numpy(), q_o) and s.cpu().numpy()[0] == s_o
+    head = dh.DraftHead(dh.DH_FMT_FP8, wl.V, q, idx, wl.n_kept, scale=s)
+    for M in (1, 4):
+        h = syn.hidden_bf16(syn.hidden_seed(2, M), M, wl.K)
+        run_step(head, h, oracle.FMT_FP8, q_o, None, s_o, wl.idx, wl.n_kept, wl.V, f"fp8 98k M={M}")
+
+
+def test_bf16_full_vocabulary_head(W_full, W_dev):
+    head = dh.bf16_full_head(W_dev)
+    for step in range(2):
+        h = syn.hidden_bf16(syn.hidden_seed(4, step), 1, W_full.shape[1])
+        ids = head.top_tokens(dev_bf16(h)).cpu().numpy()
+        y, A = oracle.gemv(oracle.FMT_BF16, W_full, None, None, h)
+        check_argmax_rows(ids, y, A, W_full.shape[0], f"bf16 full step {step}")

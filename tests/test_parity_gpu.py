@@ -1,0 +1,204 @@
+"""GPU path vs the CPU oracle, element by element, through the C ABI.
+
+Bit-exact: quantised codes, block scales, global / per-tensor scales, dh_idx,
+ids (up to near-ties) and the -inf layout of compute_logits. Logits: within
+2e-3 * sum|w' h| + 1e-5 of the oracle's fp64 value."""
+import numpy as np
+import pytest
+import torch
+
+import nvfp4_draft_head_gb300 as dh
+import oracle
+import synthetic as syn
+from parity_util import Workload, check_argmax_rows, check_logits, ids_to_rows, plant_near_ties
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    from nvfp4_draft_head_gb300 import build
+    build.build()
+    dh.lib()
+
+
+def dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def dev_bf16(bits):
+    return dev(bits.view(np.int16)).view(torch.bfloat16)
+
+
+@pytest.fixture(scope="module")
+def tiny():
+    c = syn.TINY
+    return Workload(syn.SEED_HEAD_TINY, c["V"], c["K"], c["n_kept"], c["forced"], syn.SEED_KEEP_TINY)
+
+
+def gpu_nvfp4(wl):
+    W = dev_bf16(wl.W)
+    idx = dev(wl.idx)
+    q, sf, g = dh.nvfp4_quantize_rows(W, idx)
+    return dh.DraftHead(dh.DH_FMT_NVFP4, wl.V, q, idx, wl.n_kept, sf=sf, scale=g), (q, sf, g)
+
+
+def gpu_fp8(wl):
+    W = dev_bf16(wl.W)
+    idx = dev(wl.idx)
+    q, s = dh.fp8_quantize_rows(W, idx)
+    return dh.DraftHead(dh.DH_FMT_FP8, wl.V, q, idx, wl.n_kept, scale=s), (q, s)
+
+
+def run_step(head, h_bits, fmt, q_or, sf_or, s_or, idx, n_kept, V, what):
+    """top_tokens + compute_logits for one batch of hidden rows, both checked."""
+    h = dev_bf16(h_bits)
+    M = h_bits.shape[0]
+    top = torch.empty(M, dtype=torch.float32, device="cuda")
+    ids = head.top_tokens(h, top=top).cpu().numpy()
+    out = head.compute_logits(h).cpu().numpy()
+    assert head.device_error() == 0
+    y, A = oracle.gemv(fmt, q_or, sf_or, s_or, h_bits)
+    rows = ids_to_rows(ids, idx, n_kept) if idx is not None else ids
+    exact = check_argmax_rows(rows, y, A, n_kept, what)
+    check_logits(top.cpu().numpy()[:, None], y[np.arange(M), rows][:, None],
+                 A[np.arange(M), rows][:, None], what + " top logit")
+    ref = oracle.scatter_logits(y, idx if idx is not None else np.arange(y.shape[1], dtype=np.int32),
+                                n_kept, V)
+    assert np.array_equal(np.isneginf(out), np.isneginf(ref)), what + " -inf layout"
+    fin = np.isfinite(ref)
+    assert np.isfinite(out[fin]).all()
+    kept_ids = (idx if idx is not None else np.arange(n_kept))[:n_kept]
+    rel = check_logits(out[:, kept_ids], y[:, :n_kept], A[:, :n_kept], what + " logits")
+    return exact, rel
+
+
+# ------------------------------------------------------------------ tiny ----
+
+def test_tiny_nvfp4_quantize_bit_exact(tiny):
+    _, (q, sf, g) = gpu_nvfp4(tiny)
+    q_o, sf_o, g_o = tiny.nvfp4()
+    assert np.array_equal(q.cpu().numpy(), q_o)
+    assert np.array_equal(sf.cpu().numpy(), sf_o)
+    assert g.cpu().numpy()[0] == g_o
+
+
+def test_tiny_fp8_quantize_bit_exact(tiny):
+    _, (q, s) = gpu_fp8(tiny)
+    q_o, s_o = tiny.fp8()
+    assert np.array_equal(q.cpu().numpy(), q_o)
+    assert s.cpu().numpy()[0] == s_o
+
+
+@pytest.mark.parametrize("M", [1, 2, 3, 4, 8, 13, 16])
+def test_tiny_nvfp4_step(tiny, M):
+    head, _ = gpu_nvfp4(tiny)
+    q_o, sf_o, g_o = tiny.nvfp4()
+    for step in range(3):
+        h = syn.hidden_bf16(syn.hidden_seed(0, 100 * M + step), M, tiny.K)
+        run_step(head, h, oracle.FMT_NVFP4, q_o, sf_o, g_o, tiny.idx, tiny.n_kept, tiny.V,
+                 f"tiny nvfp4 M={M} step={step}")
+
+
+@pytest.mark.parametrize("M", [1, 4, 16])
+def test_tiny_fp8_step(tiny, M):
+    head, _ = gpu_fp8(tiny)
+    q_o, s_o = tiny.fp8()
+    h = syn.hidden_bf16(syn.hidden_seed(0, 500 + M), M, tiny.K)
+    run_step(head, h, oracle.FMT_FP8, q_o, None, s_o, tiny.idx, tiny.n_kept, tiny.V, f"tiny fp8 M={M}")
+
+
+@pytest.mark.parametrize("M", [1, 2, 16])
+def test_tiny_bf16_full_head_step(tiny, M):
+    W = dev_bf16(tiny.W)
+    head = dh.bf16_full_head(W)
+    h = syn.hidden_bf16(syn.hidden_seed(0, 700 + M), M, tiny.K)
+    run_step(head, h, oracle.FMT_BF16, tiny.W, None, None, None, tiny.V, tiny.V, f"tiny bf16 M={M}")
+
+
+@pytest.mark.parametrize("V,K,n_kept,forced", [
+    (64, 256, 1, 1),          # one kept id: N = 64, 63 padding rows
+    (4096, 256, 4096, 0),     # every id kept: a plain full-vocabulary argmax
+    (1000, 256, 65, 3),       # ragged: 65 kept -> 128 rows
+    (3000, 5120, 700, 10),    # the larger hidden size
+    (2000, 2560, 129, 1),     # pages' hidden size, small ragged head
+])
+def test_edge_shapes(V, K, n_kept, forced):
+    wl = Workload(77 + K, V, K, n_kept, forced, 88 + n_kept)
+    head, (q, sf, g) = gpu_nvfp4(wl)
+    q_o, sf_o, g_o = wl.nvfp4()
+    assert np.array_equal(q.cpu().numpy(), q_o) and np.array_equal(sf.cpu().numpy(), sf_o)
+    assert g.cpu().numpy()[0] == g_o
+    for M in (1, 5):
+        h = syn.hidden_bf16(900 + M + K, M, K)
+        run_step(head, h, oracle.FMT_NVFP4, q_o, sf_o, g_o, wl.idx, wl.n_kept, V, f"edge V={V} K={K} M={M}")
+    head8, (q8, s8) = gpu_fp8(wl)
+    q8_o, s8_o = wl.fp8()
+    assert np.array_equal(q8.cpu().numpy(), q8_o) and s8.cpu().numpy()[0] == s8_o
+    run_step(head8, syn.hidden_bf16(950 + K, 3, K), oracle.FMT_FP8, q8_o, None, s8_o, wl.idx,
+             wl.n_kept, V, f"edge fp8 V={V} K={K}")
+
+
+def test_special_hidden_states(tiny):
+    head, _ = gpu_nvfp4(tiny)
+    q_o, sf_o, g_o = tiny.nvfp4()
+    K = tiny.K
+    h = np.zeros((4, K), np.uint16)
+    h[1, 17] = syn.f32_to_bf16_bits(np.float32([1.0]))[0]          # one-hot: reads one column
+    h[2] = syn.f32_to_bf16_bits(np.full(K, 3.0e4, np.float32))      # large values (f16 prescale)
+    h[3] = syn.hidden_bf16(5, 1, K)[0]
+    h[3, ::2] = 0
+    run_step(head, h, oracle.FMT_NVFP4, q_o, sf_o, g_o, tiny.idx, tiny.n_kept, tiny.V, "special h")
+    # an all-zero hidden state: every logit is 0, the first kept row (id idx[0]) wins
+    ids = head.top_tokens(dev_bf16(h[:1])).cpu().numpy()
+    assert ids[0] == tiny.idx[0]
+
+
+def test_same_hidden_rows_agree(tiny):
+    head, _ = gpu_nvfp4(tiny)
+    h = np.repeat(syn.hidden_bf16(11, 1, tiny.K), 6, axis=0)
+    top = torch.empty(6, device="cuda")
+    ids = head.top_tokens(dev_bf16(h), top=top).cpu().numpy()
+    assert len(set(ids.tolist())) == 1 and len(set(top.cpu().numpy().tolist())) == 1
+    out = head.compute_logits(dev_bf16(h)).cpu().numpy()
+    assert all(np.array_equal(out[0], out[i]) for i in range(6))
+
+
+def test_cuda_graph_replay(tiny):
+    head, _ = gpu_nvfp4(tiny)
+    q_o, sf_o, g_o = tiny.nvfp4()
+    M = 2
+    h_static = torch.empty((M, tiny.K), dtype=torch.bfloat16, device="cuda")
+    ids_static = torch.empty(M, dtype=torch.int32, device="cuda")
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        head.top_tokens(h_static.zero_(), ids=ids_static)    # warm-up outside capture
+    torch.cuda.current_stream().wait_stream(s)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        head.top_tokens(h_static, ids=ids_static)
+    for step in range(5):
+        hb = syn.hidden_bf16(syn.hidden_seed(0, 9000 + step), M, tiny.K)
+        h_static.copy_(dev_bf16(hb))
+        graph.replay()
+        ids = ids_static.cpu().numpy()
+        y, A = oracle.gemv(oracle.FMT_NVFP4, q_o, sf_o, g_o, hb)
+        check_argmax_rows(ids_to_rows(ids, tiny.idx, tiny.n_kept), y, A, tiny.n_kept, f"graph {step}")
+        eager = head.top_tokens(dev_bf16(hb)).cpu().numpy()
+        assert np.array_equal(ids, eager)
+
+
+def test_out_of_range_idx_sets_the_error_word(tiny):
+    head, (q, sf, g) = gpu_nvfp4(tiny)
+    bad = tiny.idx.copy()
+    bad[5] = tiny.V            # one kept row points past the vocabulary
+    idx_bad = dev(bad)
+    head_bad = dh.DraftHead(dh.DH_FMT_NVFP4, tiny.V, q, idx_bad, tiny.n_kept, sf=sf, scale=g)
+    h = dev_bf16(syn.hidden_bf16(3, 1, tiny.K))
+    head_bad.compute_logits(h)
+    assert head_bad.device_error() == dh.DH_DEVERR_IDX
+    assert head_bad.device_error() == 0                        # reading clears it
+    with pytest.raises(RuntimeError, match="device error"):
+        dh.nvfp4_quantize_rows(dev_bf16(tiny.W), idx_bad)
