@@ -1,0 +1,363 @@
+"""Benchmark of the draft step: NVFP4 64,064 x 2560 head GEMV + argmax, M = 1.
+
+One step = one draft_head_top_tokens call (GEMV + argmax + dh_idx map) on a
+fresh BF16 hidden state. Workload: V = 248,320, K = 2560, 64,026 kept ids
+padded to 64,064 rows. L2 (129 MB) is defeated by rotating six copies of the
+92.25 MB head (553.5 MB). The K timed steps are captured in one CUDA graph
+(as a drafter replays its draft loop) and timed with CUDA events on the
+launching stream; value = µs per draft step.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl reference times the CPU oracle (the only baseline here) on the same
+workload: each step computes a bounded sample of the head's rows in fp64 and
+is scaled to a full step.
+With N > 1 (torchrun) every rank runs an independent replica (the draft head
+does not shard on one box); value = max-over-ranks time / (N * K).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synthetic as syn  # noqa: E402
+
+METRIC = "µs/draft step & HBM GB/s, NVFP4 64,064×2560 head GEMV+argmax, M=1"
+WORKLOAD = "nvfp4 draft head 64,064x2560 (V=248,320, 64,026 kept), GEMV+argmax, M=1"
+COPIES = 6
+FALLBACK_HBM_GBS = 6800.0
+
+# Algorithmic bytes of one draft step at M = 1: NVFP4 codes (64,064 x 1,280 B)
+# + E4M3 block scales (64,064 x 160 B) + g (4 B) + h (2,560 x 2 B) + the id (4 B).
+# dh_idx is read only for the winning row.
+N_ROWS, K_HID = 64_064, 2_560
+STEP_BYTES = N_ROWS * (K_HID // 2) + N_ROWS * (K_HID // 16) + 4 + 2 * K_HID + 4
+
+# DRAM traffic of one launch of the GEMV kernel from an ncu capture, valid
+# while the kernel source hashes to KERNEL_SHA (else reported as null).
+TRAFFIC = {"kernel_sha": None, "bytes_per_launch": None}
+
+
+def kernel_sha() -> str:
+    h = hashlib.sha256()
+    for f in ("dh_gemv_impl.cuh", "dh_common.cuh", "dh_gemv_nvfp4.cu"):
+        with open(os.path.join(ROOT, "nvfp4_draft_head_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def hbm_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples while the GPU is under load."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.rows = []
+        self.proc = None
+        self.t = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.t = threading.Thread(target=self._read, daemon=True)
+        self.t.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append([x.strip() for x in line.split(",")])
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.t.join(timeout=2)
+        sm = [float(r[1]) for r in self.rows if len(r) >= 9 and r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in self.rows if len(r) >= 9 and r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in self.rows if len(r) >= 9
+                          for i in range(4) if r[5 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(sm)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def workload_host():
+    c = syn.QWEN_64K
+    W = syn.head_bf16(syn.SEED_HEAD_QWEN, c["V"], c["K"])
+    keep = syn.keep_mask(syn.SEED_KEEP_64K, c["V"], c["n_kept"], c["forced"])
+    return W, keep
+
+
+def hidden_steps(n):
+    return np.concatenate([syn.hidden_bf16(syn.hidden_seed(1, i), 1, K_HID) for i in range(n)])
+
+
+def oracle_sample_steps(q, sf, g, hs, n_steps, sample_rows, budget_s=None):
+    """Time the oracle's draft step on a bounded sample: step i computes the
+    fp64 logits and argmax of `sample_rows` consecutive head rows (a rotating
+    window); returns (seconds per full step, steps done)."""
+    import oracle
+    n_win = N_ROWS // sample_rows
+    t_total, done = 0.0, 0
+    for i in range(n_steps):
+        w = i % n_win
+        r0 = w * sample_rows
+        h = hs[i % hs.shape[0]][None]
+        t0 = time.perf_counter()
+        y, _ = oracle.gemv(oracle.FMT_NVFP4, q[r0:r0 + sample_rows], sf[r0:r0 + sample_rows], g, h,
+                           want_abs=False)
+        oracle.top_tokens(y, None)
+        t_total += time.perf_counter() - t0
+        done += 1
+        if budget_s is not None and t_total >= budget_s:
+            break
+    return t_total / done * (N_ROWS / sample_rows), done
+
+
+def emit(obj):
+    print(json.dumps(obj), flush=True)
+
+
+def run_reference(args, world, rank):
+    """The CPU oracle on this host's cores, same workload, metric and unit."""
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    W, keep = workload_host()
+    idx, nk = oracle.build_index(keep)
+    q, sf, g = oracle.nvfp4_quantize(W, idx)
+    hs = hidden_steps(min(64, args.warmup + args.steps))
+    sample = N_ROWS // 16
+    oracle_sample_steps(q, sf, g, hs, args.warmup, sample)
+    sec, done = oracle_sample_steps(q, sf, g, hs, args.steps, sample)
+    us = sec * 1e6
+    cpu = {"value": us, "unit": "us/step", "cores": 1, "kind": "oracle",
+           "sample": f"each step: fp64 GEMV+argmax over {sample} of {N_ROWS} rows (rotating window), "
+                     f"scaled x{N_ROWS // sample}"}
+    emit({"impl": "reference", "metric": METRIC, "value": us, "unit": "us/step", "n_gpus": world,
+          "steps": done, "warmup": args.warmup, "ms_per_step": us / 1e3, "higher_is_better": False,
+          "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+          "config": {"workload": WORKLOAD, "M": 1, "V": 248_320, "K": K_HID, "N": N_ROWS,
+                     "n_kept": nk},
+          "cpu_baseline": cpu,
+          "e2e": {"value": us, "unit": "us/step", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}})
+
+
+def run_ours(args, world, rank, local):
+    import torch
+
+    import nvfp4_draft_head_gb300 as dh
+    from nvfp4_draft_head_gb300 import build
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as tdist
+        tdist.init_process_group("nccl", device_id=dev)
+    build.build()
+    lib_loaded = dh.lib()
+
+    W, keep = workload_host()
+    Wd = torch.from_numpy(W.view(np.int16)).to(dev).view(torch.bfloat16)
+    head = dh.nvfp4_head(Wd, keep)
+    del Wd
+    heads = [head] + [head.with_storage(head.q.clone(), head.sf.clone()) for _ in range(COPIES - 1)]
+    K, Wm = args.steps, args.warmup
+    hs_host = hidden_steps(Wm + K)
+    hs = torch.from_numpy(hs_host.view(np.int16)).to(dev).view(torch.bfloat16)
+    ids = torch.empty((Wm + K, 1), dtype=torch.int32, device=dev)
+    torch.cuda.synchronize()
+
+    # Parity first (rank 0): quantised bytes bit-exact; the ids of the first steps
+    # within the oracle's tolerance rule.
+    parity = None
+    if rank == 0:
+        import oracle
+        oracle.build()
+        idx_o, nk = oracle.build_index(keep)
+        q_o, sf_o, g_o = oracle.nvfp4_quantize(W, idx_o)
+        exact = (np.array_equal(head.q.cpu().numpy(), q_o) and np.array_equal(head.sf.cpu().numpy(), sf_o)
+                 and head.scale.cpu().numpy()[0] == g_o)
+        n_chk = 3
+        for i in range(n_chk):
+            heads[i % COPIES].top_tokens(hs[i:i + 1], ids=ids[i])
+        got = ids[:n_chk, 0].cpu().numpy()
+        ok = True
+        for i in range(n_chk):
+            y, A = oracle.gemv(oracle.FMT_NVFP4, q_o, sf_o, g_o, hs_host[i:i + 1])
+            r = int(np.argmax(y[0, :nk]))
+            j = int(np.nonzero(idx_o[:nk] == got[i])[0][0]) if got[i] in idx_o[:nk] else -1
+            t = lambda n: 2e-3 * A[0, n] + 1e-5
+            ok &= (j == r) or (j >= 0 and y[0, r] - y[0, j] <= t(r) + t(j))
+        parity = {"quantize_bit_exact": bool(exact), "steps_checked": n_chk, "ids_within_tolerance": bool(ok)}
+        del W
+        if not (exact and ok):
+            emit({"error": "parity failed before timing", "parity": parity})
+            sys.exit(1)
+    else:
+        del W
+
+    s = torch.cuda.Stream(device=dev)
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        for i in range(Wm):                               # untimed warm-up steps
+            heads[i % COPIES].top_tokens(hs[i:i + 1], ids=ids[i])
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=s):
+            for i in range(Wm, Wm + K):
+                heads[i % COPIES].top_tokens(hs[i:i + 1], ids=ids[i])
+        graph.replay()                                    # untimed: uploads the graph
+    s.synchronize()
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    t_end = time.perf_counter() + 1.5                     # sustained load around the timed region
+    with torch.cuda.stream(s):
+        while time.perf_counter() < t_end:
+            graph.replay()
+            s.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(s)
+        graph.replay()
+        e1.record(s)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1)
+        for _ in range(3):                                # keep load on while the sampler catches up
+            graph.replay()
+        s.synchronize()
+    clocks = sampler.stop()
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+        torch.distributed.barrier()
+    assert head.device_error() == 0
+
+    # End to end through the public call with host buffers: per step, copy the
+    # hidden state from pinned host memory, run the draft step, read the id back.
+    h_pin = torch.from_numpy(hs_host.view(np.int16)).view(torch.bfloat16).pin_memory()
+    ids_pin = torch.empty((Wm + K, 1), dtype=torch.int32).pin_memory()
+    h_dev = torch.empty((1, K_HID), dtype=torch.bfloat16, device=dev)
+    id_dev = torch.empty(1, dtype=torch.int32, device=dev)
+    with torch.cuda.stream(s):
+        for i in range(Wm):
+            h_dev.copy_(h_pin[i:i + 1], non_blocking=True)
+            heads[i % COPIES].top_tokens(h_dev, ids=id_dev)
+            ids_pin[i].copy_(id_dev, non_blocking=True)
+        torch.cuda.synchronize()
+        f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        f0.record(s)
+        for i in range(Wm, Wm + K):
+            h_dev.copy_(h_pin[i:i + 1], non_blocking=True)
+            heads[i % COPIES].top_tokens(h_dev, ids=id_dev)
+            ids_pin[i].copy_(id_dev, non_blocking=True)
+        f1.record(s)
+        torch.cuda.synchronize()
+        ms_e2e = f0.elapsed_time(f1)
+    if world > 1:
+        t = torch.tensor([ms_e2e], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms_e2e = float(t.item())
+    e2e_ok = bool(np.array_equal(ids_pin[Wm:].numpy(), ids[Wm:].cpu().numpy()))
+
+    cpu = None
+    if rank == 0 and world == 1:
+        sec, done = oracle_sample_steps(q_o, sf_o, g_o, hs_host, 10_000, N_ROWS // 16, budget_s=12.0)
+        cpu = {"value": sec * 1e6, "unit": "us/step", "cores": 1, "kind": "oracle",
+               "sample": f"{done} steps, each an fp64 GEMV+argmax over {N_ROWS // 16} of {N_ROWS} rows "
+                         f"(rotating window) scaled x16; single-threaded C"}
+
+    if rank != 0:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return
+    us_step = ms * 1e3 / K
+    value = us_step / world
+    gbs = STEP_BYTES / (us_step * 1e-6) / 1e9
+    peak, peak_src = hbm_peak()
+    sha = kernel_sha()
+    traffic = TRAFFIC["bytes_per_launch"] if TRAFFIC["kernel_sha"] == sha else None
+    emit({"metric": METRIC, "value": value, "unit": "us/step", "n_gpus": world, "steps": K, "warmup": Wm,
+          "ms_per_step": us_step / 1e3, "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
+          "dtype": "f32", "data": "synthetic",
+          "config": {"workload": WORKLOAD, "M": 1, "V": 248_320, "K": K_HID, "N": N_ROWS, "n_kept": 64_026,
+                     "head_copies": COPIES, "l2": "inputs larger than L2: 6 rotating head copies "
+                     "(553.5 MB > 4 x 129 MB)", "timing": "one CUDA graph of K steps, CUDA events",
+                     "parallelism": "replicas" if world > 1 else "single"},
+          "hbm_gbs": gbs,
+          "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "peak_source": peak_src,
+                       "unit": "GB/s", "frac": gbs / peak, "traffic": traffic,
+                       "kernel": "gemv_kernel<NVFP4, 2560, M=1> (top tokens)",
+                       "bytes_per_launch": STEP_BYTES},
+          "cpu_baseline": cpu,
+          "e2e": {"value": ms_e2e * 1e3 / K / world, "unit": "us/step", "h2d_bytes_per_step": 2 * K_HID,
+                  "d2h_bytes_per_step": 4, "ids_match_graph": e2e_ok},
+          "gpu_launches": K, "clocks": clocks, "parity": parity,
+          "library": os.path.relpath(dh.library_path(), ROOT), "kernel_sha": sha})
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    del lib_loaded
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+    else:
+        run_ours(args, world, rank, local)
+
+
+if __name__ == "__main__":
+    main()

@@ -72,9 +72,12 @@ class Workload:
 
 
 def plant_near_ties(q, sf, g, h_bits, n_kept, frac, seed, max_tries=8):
-    """Shift a fraction of hidden rows so that their top-2 oracle logits are
-    within 1e-3 (fp64 projection onto w'_a - w'_b, then BF16 rounding; retried
-    with a new gap up to max_tries times). Returns (h_bits, planted rows, gaps)."""
+    """Move a fraction of hidden rows so that their top-2 oracle logits (over the
+    kept rows) are within 1e-3. Each try takes the current top-2 rows a, b and
+    shifts one hidden element k by (gap - target) / (w'_a[k] - w'_b[k]), with
+    the target gap drawn from U(1e-4, 9e-4); k is the element with the smallest
+    |w'_a[k] - w'_b[k]| that keeps the shift within 2, so that rounding the new
+    value to BF16 moves the gap little. Returns (h_bits, planted rows, gaps)."""
     rng = np.random.default_rng(seed)
     h = h_bits.copy()
     M = h.shape[0]
@@ -84,18 +87,20 @@ def plant_near_ties(q, sf, g, h_bits, n_kept, frac, seed, max_tries=8):
         for _ in range(max_tries):
             y, _ = oracle.gemv(oracle.FMT_NVFP4, q, sf, g, h[m:m + 1], want_abs=False)
             order = np.argsort(-y[0, :n_kept], kind="stable")
-            a, b = order[0], order[1]
+            a, b = int(order[0]), int(order[1])
+            gap = y[0, a] - y[0, b]
+            if gap < 1e-3:
+                planted.append(int(m))
+                gaps.append(float(gap))
+                break
             wab = oracle.dequant_nvfp4(q[[a, b]], sf[[a, b]], g)
             d = wab[0] - wab[1]
-            delta = rng.uniform(0, 1e-3)
-            x = syn.bf16_bits_to_f32(h[m]).astype(np.float64)
-            x -= (y[0, a] - y[0, b] - delta) / (d @ d) * d
-            cand = syn.f32_to_bf16_bits(x.astype(np.float32))
-            y2, _ = oracle.gemv(oracle.FMT_NVFP4, q, sf, g, cand[None], want_abs=False)
-            top2 = np.sort(y2[0, :n_kept])[-2:]
-            if top2[1] - top2[0] < 1e-3:
-                h[m] = cand
-                planted.append(int(m))
-                gaps.append(float(top2[1] - top2[0]))
+            move = gap - rng.uniform(1e-4, 9e-4)
+            ok = np.abs(d) >= move / 2.0
+            if not ok.any():
                 break
+            k = int(np.argmin(np.where(ok, np.abs(d), np.inf)))
+            x = syn.bf16_bits_to_f32(h[m]).astype(np.float64)
+            x[k] -= move / d[k]
+            h[m] = syn.f32_to_bf16_bits(x.astype(np.float32))
     return h, planted, gaps
