@@ -157,6 +157,24 @@ int draft_head_top_tokens(const dh_head_t *hd, const void *h, int M, int32_t *id
 int draft_head_compute_logits(const dh_head_t *hd, const void *h, int M, float *out,
                               void *ws, size_t ws_bytes, void *stream);
 
+/* get_top_tokens without a caller workspace, for callers that cannot
+ * allocate device memory: a plugin hook that is handed only its input and
+ * output buffers, or a serving loop that forbids cudaMalloc because it can
+ * synchronise the device. The paper has no counterpart of this entry point.
+ * Same arguments and results as draft_head_top_tokens, minus the workspace.
+ * Its scratch is one fixed 256-byte array inside the library (argmax keys for
+ * at most DH_MAX_M = 16 drafts, a ticket, an error word); every GPU that loads
+ * the library holds it until the process exits. M > 16 returns DH_ERR_SHAPE.
+ * The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call
+ * before any stream capture. Each call clears the keys and the ticket with
+ * cudaMemsetAsync on `stream`, then launches the kernel; nothing is allocated.
+ * All calls share the one array, so calls that overlap on the GPU (other
+ * streams, other threads) race and give wrong ids: serialise them. An id of
+ * -1 marks a winning row whose dh_idx entry was outside [0, V). */
+int draft_head_top_tokens_static(const dh_head_t *hd, const void *h, int M, int32_t *ids,
+                                 float *top_logit, void *stream);
+
 /* Synchronise `stream`, then read and clear the device error word of `ws`
  * (draft-step or quantiser workspace). *err = 0 when nothing was recorded. */
 int draft_head_read_device_error(void *ws, int *err, void *stream);

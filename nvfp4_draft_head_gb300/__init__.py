@@ -31,7 +31,7 @@ EXPORTS = (
     "draft_head_build_index", "draft_head_quantize_workspace_bytes", "nvfp4_quantize_rows",
     "fp8_quantize_rows", "draft_head_workspace_bytes", "draft_head_workspace_init",
     "draft_head_top_tokens", "draft_head_compute_logits", "draft_head_read_device_error",
-    "draft_head_status_string", "draft_head_abi_version",
+    "draft_head_status_string", "draft_head_abi_version", "draft_head_top_tokens_static",
 )
 
 _lib = None
@@ -78,6 +78,7 @@ def lib():
         L.draft_head_status_string.argtypes = [I]
         L.draft_head_status_string.restype = C.c_char_p
         L.draft_head_abi_version.argtypes = []
+        L.draft_head_top_tokens_static.argtypes = [C.POINTER(dh_head_t), P, I, P, P, P]
         _lib = L
     return _lib
 
