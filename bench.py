@@ -212,7 +212,7 @@ def run_ours(args, world, rank, local):
     # Parity first (rank 0): quantised bytes bit-exact; the ids of the first steps
     # within the oracle's tolerance rule.
     parity = None
-    if rank == 0:
+    if rank == 0 and not args.profile:
         import oracle
         oracle.build()
         idx_o, nk = oracle.build_index(keep)
@@ -240,6 +240,17 @@ def run_ours(args, world, rank, local):
 
     s = torch.cuda.Stream(device=dev)
     s.wait_stream(torch.cuda.current_stream())
+    if args.profile:
+        # Short run for a profiler: W + K eager steps over the rotating copies,
+        # nothing else (no graph, no clock sampling, no end-to-end leg).
+        with torch.cuda.stream(s):
+            for i in range(Wm + K):
+                heads[i % COPIES].top_tokens(hs[i:i + 1], ids=ids[i])
+        s.synchronize()
+        assert head.device_error() == 0
+        if rank == 0:
+            emit({"profile_run": True, "steps": K, "warmup": Wm})
+        return
     with torch.cuda.stream(s):
         for i in range(Wm):                               # untimed warm-up steps
             heads[i % COPIES].top_tokens(hs[i:i + 1], ids=ids[i])
@@ -349,6 +360,8 @@ def main():
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--profile", action="store_true",
+                    help="eager steps only, for ncu (prints no measurement)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -314,6 +314,192 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const GemvArgs a) {
     }
 }
 
+// ------------------------------------------------------- pipelined, M = 1 ----
+//
+// Persistent variant for one draft. A producer warp streams "chunks" of NCW
+// consecutive groups (their code bytes and E4M3 scale bytes, both contiguous
+// in the head) into an S-stage shared-memory ring with 1-D bulk async copies
+// (cp.async.bulk, completion counted on an mbarrier per stage), so that
+// S * chunk bytes per SM are in flight regardless of registers. NCW consumer
+// warps each take one group of a chunk: they copy their slots from shared
+// memory to registers (the same conflict-free 512-byte rows as the direct
+// path), release the stage, and dequantise / dot / reduce as in gemv_kernel.
+// CTA c owns chunks c, c + grid, c + 2 grid, ... Every wait is bounded: on a
+// timeout the CTA records kDevErrTimeout, stops, waits (bounded) for its
+// copies in flight and still takes part in the argmax hand-off.
+template <int FMT, int K, int NCW, int S, bool LOGITS>
+__global__ void __launch_bounds__((NCW + 1) * 32, 1) gemv_pipe_kernel(const GemvArgs a) {
+    using G = Geom<FMT, K>;
+    constexpr int R = G::R, L = G::L, RB = G::RB, HREG = G::HREG, EPU = G::EPU;
+    constexpr int C = NCW;                              // groups per chunk
+    constexpr int GQ = R * RB;                          // code bytes per group (512 L)
+    constexpr int GS = (FMT == 1) ? R * G::SFB : 0;     // scale bytes per group (64 L)
+    constexpr int STAGE = C * (GQ + GS);
+    constexpr int KW = K / 2;
+    constexpr int NC = NCW * 32;                        // consumer threads
+    static_assert(GQ % 16 == 0 && GS % 16 == 0, "bulk copies move multiples of 16 bytes");
+    extern __shared__ __align__(128) uint8_t smem[];
+    uint8_t* ring = smem;
+    uint32_t* s_hw = reinterpret_cast<uint32_t*>(smem + S * STAGE);
+    __shared__ __align__(8) uint64_t full[S];
+    __shared__ __align__(8) uint64_t empty[S];
+    __shared__ float s_red[NCW];
+    __shared__ unsigned long long s_key[NCW];
+    __shared__ unsigned long long s_cta[1];
+    __shared__ int s_abort;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int n_groups = a.N / R;
+    const int n_chunks = (n_groups + C - 1) / C;
+    const int my_chunks = static_cast<int>(blockIdx.x) < n_chunks
+                              ? (n_chunks - 1 - static_cast<int>(blockIdx.x)) / static_cast<int>(gridDim.x) + 1
+                              : 0;
+    volatile int* abort_flag = &s_abort;
+
+    if (tid == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], NCW);
+        }
+        s_abort = 0;
+        mbar_init_fence();
+    }
+    __syncthreads();
+
+    unsigned long long best = 0ull;
+    if (warp == NCW) {
+        // ---------------- producer ----------------
+        if (lane == 0) {
+            const uint64_t pol = policy_evict_first();
+            const uint8_t* qb = static_cast<const uint8_t*>(a.q);
+            int issued = 0;
+            for (int i = 0; i < my_chunks; ++i) {
+                const int s = i % S;
+                if (i >= S && !mbar_wait(&empty[s], ((i / S) - 1) & 1)) {
+                    atomicOr(&a.ws->error, kDevErrTimeout);
+                    *abort_flag = 1;
+                }
+                if (*abort_flag) break;
+                const int g0 = (static_cast<int>(blockIdx.x) + i * static_cast<int>(gridDim.x)) * C;
+                const int ng = min(C, n_groups - g0);
+                uint8_t* st = ring + s * STAGE;
+                mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(ng * (GQ + GS)));
+                bulk_g2s(st, qb + static_cast<size_t>(g0) * GQ, static_cast<uint32_t>(ng * GQ), &full[s], pol);
+                if constexpr (FMT == 1)
+                    bulk_g2s(st + C * GQ, a.sf + static_cast<size_t>(g0) * GS, static_cast<uint32_t>(ng * GS),
+                             &full[s], pol);
+                ++issued;
+            }
+            if (*abort_flag) {  // let the copies already issued land before the CTA exits
+                for (int i = issued > S ? issued - S : 0; i < issued; ++i) (void)mbar_wait(&full[i % S], (i / S) & 1);
+            }
+        }
+        __syncwarp();
+    } else {
+        // ---------------- consumers ----------------
+        const uint32_t* h32 = reinterpret_cast<const uint32_t*>(a.h);
+        float am = 0.0f;
+        for (int i = tid; i < KW; i += NC) {
+            const uint32_t w = __ldg(h32 + i);
+            am = fmaxf(am, fmaxf(fabsf(bf16_lo(w)), fabsf(bf16_hi(w))));
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) am = fmaxf(am, __shfl_xor_sync(0xFFFFFFFFu, am, o));
+        if (lane == 0) s_red[warp] = am;
+        named_bar_sync(1, NC);
+        am = s_red[0];
+#pragma unroll
+        for (int w = 1; w < NCW; ++w) am = fmaxf(am, s_red[w]);
+        const int e = (FMT == 3) ? 0 : f16_prescale_exponent(am);
+        const float sc = exp2i(e);
+        for (int i = tid; i < KW; i += NC) {
+            const uint32_t w = __ldg(h32 + i);
+            s_hw[i] = pack_h<FMT>(bf16_lo(w) * sc, bf16_hi(w) * sc);
+        }
+        named_bar_sync(1, NC);
+        int rowj[L];
+        uint32_t hr[L][HREG];
+#pragma unroll
+        for (int j = 0; j < L; ++j) {
+            const int o = 512 * j + 16 * lane;
+            rowj[j] = o / RB;
+            const int wofs = ((o % RB) * EPU / 16) / 2;
+#pragma unroll
+            for (int i = 0; i < HREG; ++i) hr[j][i] = s_hw[wofs + i];
+        }
+        const float mul = (FMT == 3 ? 1.0f : __ldg(a.scale)) * exp2i(-e);
+
+        for (int i = 0; i < my_chunks; ++i) {
+            const int s = i % S;
+            if (!mbar_wait(&full[s], (i / S) & 1)) {
+                atomicOr(&a.ws->error, kDevErrTimeout);
+                *abort_flag = 1;
+            }
+            if (*abort_flag) break;
+            const int grp = (static_cast<int>(blockIdx.x) + i * static_cast<int>(gridDim.x)) * C + warp;
+            const uint8_t* st = ring + s * STAGE;
+            uint4 c[L];
+            uint32_t sv[L];
+            const bool have = grp < n_groups;
+            if (have) {
+#pragma unroll
+                for (int j = 0; j < L; ++j) {
+                    c[j] = *reinterpret_cast<const uint4*>(st + warp * GQ + 512 * j + 16 * lane);
+                    sv[j] = 0u;
+                    if constexpr (FMT == 1)
+                        sv[j] = *reinterpret_cast<const uint16_t*>(st + C * GQ + warp * GS + 64 * j + 2 * lane);
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[s]);
+            if (!have) continue;
+            float acc[R];
+#pragma unroll
+            for (int r = 0; r < R; ++r) acc[r] = 0.0f;
+#pragma unroll
+            for (int j = 0; j < L; ++j) {
+                uint32_t cf[HREG];
+                decode_slot<FMT, HREG>(c[j], cf);
+                const uint32_t s2 = (FMT == 1) ? e4m3x2_to_f16x2(sv[j]) : 0u;
+                const float part = dot_slot<FMT, HREG>(cf, hr[j], s2);
+                if constexpr (R == 1) {
+                    acc[0] += part;
+                } else {
+#pragma unroll
+                    for (int r = 0; r < R; ++r) acc[r] += (rowj[j] == r) ? part : 0.0f;
+                }
+            }
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                float v = acc[r];
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+                const int row = grp * R + r;
+                if (row < a.n_kept) {
+                    const float y = v * mul;
+                    if constexpr (LOGITS) {
+                        if (lane == r) scatter_one(a, 0, row, y);
+                    } else {
+                        const unsigned long long k = argmax_key(ordered_key(y), static_cast<uint32_t>(row));
+                        best = k > best ? k : best;
+                    }
+                }
+            }
+        }
+    }
+    __syncthreads();
+    if constexpr (!LOGITS) {
+        if (warp < NCW && lane == 0) s_key[warp] = best;
+        __syncthreads();
+        if (tid == 0) {
+            unsigned long long k = 0ull;
+            for (int w = 0; w < NCW; ++w) k = s_key[w] > k ? s_key[w] : k;
+            s_cta[0] = k;
+        }
+        __syncthreads();
+        finish_argmax(a, s_cta);
+    }
+}
+
 // ---------------------------------------------------------------- launch ----
 
 template <int FMT, int K, int MT, bool LOGITS>
@@ -344,9 +530,44 @@ inline cudaError_t launch_one(const GemvArgs& a, cudaStream_t s) {
     return cudaGetLastError();
 }
 
+// Stages of the M = 1 ring: as many as fit in about 160 KB, between 2 and 6.
+template <int FMT, int K, int NCW>
+constexpr int pipe_stages() {
+    using G = Geom<FMT, K>;
+    constexpr int stage = NCW * (G::R * G::RB + (FMT == 1 ? G::R * G::SFB : 0));
+    constexpr int s = (160 * 1024) / stage;
+    return s < 2 ? 2 : (s > 6 ? 6 : s);
+}
+
+template <int FMT, int K, bool LOGITS>
+inline cudaError_t launch_pipe(const GemvArgs& a, cudaStream_t s) {
+    using G = Geom<FMT, K>;
+    constexpr int NCW = 8;
+    constexpr int S = pipe_stages<FMT, K, NCW>();
+    constexpr int STAGE = NCW * (G::R * G::RB + (FMT == 1 ? G::R * G::SFB : 0));
+    auto kern = gemv_pipe_kernel<FMT, K, NCW, S, LOGITS>;
+    const size_t smem = static_cast<size_t>(S) * STAGE + static_cast<size_t>(K) * 2;
+    static int configured[64] = {0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!configured[dev]) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+        if (e != cudaSuccess) return e;
+        configured[dev] = 1;
+    }
+    const int sms = sm_count();
+    if (sms <= 0) return cudaErrorInvalidDevice;
+    const int n_chunks = (a.N / G::R + NCW - 1) / NCW;
+    const int blocks = n_chunks < sms ? n_chunks : sms;
+    kern<<<blocks, (NCW + 1) * 32, smem, s>>>(a);
+    return cudaGetLastError();
+}
+
 template <int FMT, int K, bool LOGITS>
 inline cudaError_t launch_m(const GemvArgs& a, cudaStream_t s) {
-    if (a.M <= 1) return launch_one<FMT, K, 1, LOGITS>(a, s);
+    if (a.M <= 1) return launch_pipe<FMT, K, LOGITS>(a, s);
     if (a.M <= 2) return launch_one<FMT, K, 2, LOGITS>(a, s);
     if (a.M <= 4) return launch_one<FMT, K, 4, LOGITS>(a, s);
     if (a.M <= 8) return launch_one<FMT, K, 8, LOGITS>(a, s);

@@ -1,13 +1,13 @@
 // Draft-step kernels for the NVFP4 head (instantiations of dh_gemv_impl.cuh).
-#include "dh_gemv_impl.cuh"
+#include "dh_gemv_mma.cuh"
 
 namespace dh {
 
 cudaError_t launch_gemv_nvfp4(const GemvArgs& a, cudaStream_t s) {
     switch (a.K) {
-        case 256: return launch_k<1, 256>(a, s);
-        case 2560: return launch_k<1, 2560>(a, s);
-        case 5120: return launch_k<1, 5120>(a, s);
+        case 256: return mma::launch_mma_k<1, 256>(a, s);
+        case 2560: return mma::launch_mma_k<1, 2560>(a, s);
+        case 5120: return mma::launch_mma_k<1, 5120>(a, s);
         default: return cudaErrorInvalidValue;
     }
 }
