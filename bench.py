@@ -52,7 +52,7 @@ TRAFFIC = {"kernel_sha": None, "bytes_per_launch": None}
 
 def kernel_sha() -> str:
     h = hashlib.sha256()
-    for f in ("dh_gemv_impl.cuh", "dh_common.cuh", "dh_gemv_nvfp4.cu"):
+    for f in ("dh_gemv_mma.cuh", "dh_gemv_impl.cuh", "dh_common.cuh", "dh_gemv_nvfp4p.cu"):
         with open(os.path.join(ROOT, "nvfp4_draft_head_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -202,7 +202,7 @@ def run_ours(args, world, rank, local):
     Wd = torch.from_numpy(W.view(np.int16)).to(dev).view(torch.bfloat16)
     head = dh.nvfp4_head(Wd, keep)
     del Wd
-    heads = [head] + [head.with_storage(head.q.clone(), head.sf.clone()) for _ in range(COPIES - 1)]
+    heads = [head] + [head.with_storage(head.q.clone()) for _ in range(COPIES - 1)]
     K, Wm = args.steps, args.warmup
     hs_host = hidden_steps(Wm + K)
     hs = torch.from_numpy(hs_host.view(np.int16)).to(dev).view(torch.bfloat16)
@@ -217,8 +217,12 @@ def run_ours(args, world, rank, local):
         oracle.build()
         idx_o, nk = oracle.build_index(keep)
         q_o, sf_o, g_o = oracle.nvfp4_quantize(W, idx_o)
-        exact = (np.array_equal(head.q.cpu().numpy(), q_o) and np.array_equal(head.sf.cpu().numpy(), sf_o)
-                 and head.scale.cpu().numpy()[0] == g_o)
+        N_, Kh = q_o.shape
+        nwin = 2 * Kh // 128
+        packed_o = np.concatenate(
+            [q_o.reshape(N_ // 16, 16, nwin, 64).transpose(0, 2, 1, 3).reshape(N_ // 16, nwin, 1024),
+             sf_o.reshape(N_ // 16, 16, nwin, 8).transpose(0, 2, 1, 3).reshape(N_ // 16, nwin, 128)], axis=2)
+        exact = (np.array_equal(head.q.cpu().numpy(), packed_o) and head.scale.cpu().numpy()[0] == g_o)
         n_chk = 3
         for i in range(n_chk):
             heads[i % COPIES].top_tokens(hs[i:i + 1], ids=ids[i])
@@ -342,7 +346,7 @@ def run_ours(args, world, rank, local):
           "hbm_gbs": gbs,
           "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "peak_source": peak_src,
                        "unit": "GB/s", "frac": gbs / peak, "traffic": traffic,
-                       "kernel": "gemv_kernel<NVFP4, 2560, M=1> (top tokens)",
+                       "kernel": "gemv_mma_kernel<NVFP4 packed, K=2560, M=1> (top tokens)",
                        "bytes_per_launch": STEP_BYTES},
           "cpu_baseline": cpu,
           "e2e": {"value": ms_e2e * 1e3 / K / world, "unit": "us/step", "h2d_bytes_per_step": 2 * K_HID,

@@ -67,7 +67,7 @@ typedef enum {
 /* Bits of the device error word. */
 #define DH_DEVERR_IDX 1u  /* a dh_idx entry was outside [0, V) */
 
-typedef enum { DH_FMT_NVFP4 = 1, DH_FMT_FP8 = 2, DH_FMT_BF16 = 3 } dh_format;
+typedef enum { DH_FMT_NVFP4 = 1, DH_FMT_FP8 = 2, DH_FMT_BF16 = 3, DH_FMT_NVFP4_PACKED = 4 } dh_format;
 
 /* A quantised draft head. Plain descriptor: the library never owns these.
  *   fmt     DH_FMT_NVFP4: q = E2M1 codes [N][K/2], element 2i of a row in the
@@ -77,6 +77,10 @@ typedef enum { DH_FMT_NVFP4 = 1, DH_FMT_FP8 = 2, DH_FMT_BF16 = 3 } dh_format;
  *                         scale = &s (per-tensor scale, 1 float).
  *           DH_FMT_BF16:  q = BF16 weights [N][K] row-major; sf = NULL;
  *                         scale = NULL (no scaling).
+ *           DH_FMT_NVFP4_PACKED: the NVFP4 head after nvfp4_pack_head: q = the
+ *                         tile-major bytes (N * (K/2 + K/16)); sf = NULL;
+ *                         scale = &g. Same values, the layout the draft-step
+ *                         kernel streams fastest.
  *   V       target vocabulary size (width of the compute_logits rows).
  *   K       hidden size. Supported by the draft-step kernels: 256, 2560
  *           (the pages' drafter hidden size) and 5120.
@@ -131,6 +135,17 @@ int nvfp4_quantize_rows(const void *W, int V, int K, const int32_t *idx, int N,
  * Arguments as for nvfp4_quantize_rows. */
 int fp8_quantize_rows(const void *W, int V, int K, const int32_t *idx, int N,
                       uint8_t *q, float *scale, void *ws, size_t ws_bytes, void *stream);
+
+/* Repack an NVFP4 head into the tile-major layout of DH_FMT_NVFP4_PACKED,
+ * the layout Marlin-style GEMV kernels also use instead of the quantiser's
+ * row-major one ("q38_draft.py": NVFP4Linear(W, "marlin")). For each tile of
+ * 16 rows and each 128-wide k-window w (in that order), `packed` holds a
+ * 1,152-byte block: the 16 rows' code bytes 64w..64w+63 (row by row), then
+ * their scale bytes 8w..8w+7 (row by row).
+ *   q [N][K/2], sf [N][K/16] as written by nvfp4_quantize_rows; packed: device
+ *   buffer of N * (K/2 + K/16) bytes. All three 16-byte aligned; N % 16 == 0,
+ *   K % 128 == 0. One kernel on `stream`. A pure byte permutation. */
+int nvfp4_pack_head(const uint8_t *q, const uint8_t *sf, int N, int K, uint8_t *packed, void *stream);
 
 /* Bytes of workspace the draft-step calls need for up to M_max drafts. */
 size_t draft_head_workspace_bytes(const dh_head_t *hd, int M_max);

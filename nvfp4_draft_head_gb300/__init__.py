@@ -22,7 +22,7 @@ import torch
 from . import build as _build
 
 DH_OK, DH_ERR_ARG, DH_ERR_SHAPE, DH_ERR_ALIGN, DH_ERR_WORKSPACE, DH_ERR_CUDA = 0, 1, 2, 3, 4, 5
-DH_FMT_NVFP4, DH_FMT_FP8, DH_FMT_BF16 = 1, 2, 3
+DH_FMT_NVFP4, DH_FMT_FP8, DH_FMT_BF16, DH_FMT_NVFP4_PACKED = 1, 2, 3, 4
 DH_MAX_M = 16
 DH_WORKSPACE_ALIGN = 256
 DH_DEVERR_IDX = 1
@@ -32,6 +32,7 @@ EXPORTS = (
     "fp8_quantize_rows", "draft_head_workspace_bytes", "draft_head_workspace_init",
     "draft_head_top_tokens", "draft_head_compute_logits", "draft_head_read_device_error",
     "draft_head_status_string", "draft_head_abi_version", "draft_head_top_tokens_static",
+    "nvfp4_pack_head",
 )
 
 _lib = None
@@ -79,6 +80,7 @@ def lib():
         L.draft_head_status_string.restype = C.c_char_p
         L.draft_head_abi_version.argtypes = []
         L.draft_head_top_tokens_static.argtypes = [C.POINTER(dh_head_t), P, I, P, P, P]
+        L.nvfp4_pack_head.argtypes = [P, P, I, I, P, P]
         _lib = L
     return _lib
 
@@ -155,6 +157,18 @@ def fp8_quantize_rows(W: torch.Tensor, idx: torch.Tensor, stream=None):
     return q, s
 
 
+def nvfp4_pack_head(q: torch.Tensor, sf: torch.Tensor, stream=None) -> torch.Tensor:
+    """Tile-major copy of an NVFP4 head (DH_FMT_NVFP4_PACKED): uint8 [N/16, K/128, 1152]."""
+    N, Kh = q.shape
+    K = 2 * Kh
+    if sf.shape != (N, K // 16) or q.dtype != torch.uint8 or sf.dtype != torch.uint8:
+        raise ValueError("q must be uint8 [N, K/2] and sf uint8 [N, K/16]")
+    packed = torch.empty((N // 16, K // 128, 1152), dtype=torch.uint8, device=q.device)
+    _check("nvfp4_pack_head",
+           lib().nvfp4_pack_head(q.data_ptr(), sf.data_ptr(), N, K, packed.data_ptr(), _stream(stream)))
+    return packed
+
+
 def draft_head_read_device_error(ws: torch.Tensor, stream=None) -> int:
     err = C.c_int()
     _check("draft_head_read_device_error",
@@ -182,7 +196,10 @@ class DraftHead:
         self.fmt, self.V, self.n_kept = fmt, int(V), int(n_kept)
         self.q, self.sf, self.scale, self.idx = q, sf, scale, idx
         self.N = q.shape[0]
-        if fmt == DH_FMT_NVFP4:
+        if fmt == DH_FMT_NVFP4_PACKED:        # [N/16, K/128, 1152]
+            self.N = q.shape[0] * 16
+            self.K = q.shape[1] * 128
+        elif fmt == DH_FMT_NVFP4:
             self.K = q.shape[1] * 2
         elif fmt == DH_FMT_FP8:
             self.K = q.shape[1]
@@ -236,11 +253,15 @@ class DraftHead:
         return h.shape[0]
 
 
-def nvfp4_head(W: torch.Tensor, keep, stream=None) -> DraftHead:
-    """Build an NVFP4 draft head from a BF16 target head and a host keep mask."""
+def nvfp4_head(W: torch.Tensor, keep, packed: bool = True, stream=None) -> DraftHead:
+    """Build an NVFP4 draft head from a BF16 target head and a host keep mask
+    (repacked tile-major unless packed=False)."""
     idx_np, nk = draft_head_build_index(keep)
     idx = torch.from_numpy(idx_np).to(W.device)
     q, sf, g = nvfp4_quantize_rows(W, idx, stream)
+    if packed and (W.shape[1] % 128 == 0):
+        qp = nvfp4_pack_head(q, sf, stream)
+        return DraftHead(DH_FMT_NVFP4_PACKED, W.shape[0], qp, idx, nk, scale=g)
     return DraftHead(DH_FMT_NVFP4, W.shape[0], q, idx, nk, sf=sf, scale=g)
 
 

@@ -31,12 +31,13 @@ int check_gather(const void* W, int V, int K, const int32_t* idx, int N) {
 
 int check_head(const dh_head_t* hd) {
     if (hd == nullptr || hd->q == nullptr) return DH_ERR_ARG;
-    if (hd->fmt != DH_FMT_NVFP4 && hd->fmt != DH_FMT_FP8 && hd->fmt != DH_FMT_BF16) return DH_ERR_ARG;
+    if (hd->fmt != DH_FMT_NVFP4 && hd->fmt != DH_FMT_FP8 && hd->fmt != DH_FMT_BF16 && hd->fmt != DH_FMT_NVFP4_PACKED)
+        return DH_ERR_ARG;
     if (hd->V <= 0 || hd->N <= 0 || hd->n_kept < 1 || hd->n_kept > hd->N) return DH_ERR_SHAPE;
     if (hd->N % 64 != 0) return DH_ERR_SHAPE;
     if (!dh::gemv_supported(hd->fmt, hd->K)) return DH_ERR_SHAPE;
     if (hd->fmt == DH_FMT_NVFP4 && (hd->sf == nullptr || hd->scale == nullptr)) return DH_ERR_ARG;
-    if (hd->fmt == DH_FMT_FP8 && hd->scale == nullptr) return DH_ERR_ARG;
+    if ((hd->fmt == DH_FMT_FP8 || hd->fmt == DH_FMT_NVFP4_PACKED) && hd->scale == nullptr) return DH_ERR_ARG;
     if (hd->idx == nullptr) {
         if (hd->fmt != DH_FMT_BF16) return DH_ERR_ARG;
         if (hd->n_kept != hd->N || hd->N > hd->V) return DH_ERR_SHAPE;
@@ -136,6 +137,14 @@ int fp8_quantize_rows(const void* W, int V, int K, const int32_t* idx, int N, ui
     return cuda_status(dh::launch_fp8_quantize(static_cast<const uint16_t*>(W), V, K, idx, N, q, scale,
                                                static_cast<dh::Workspace*>(ws),
                                                static_cast<cudaStream_t>(stream)));
+}
+
+int nvfp4_pack_head(const uint8_t* q, const uint8_t* sf, int N, int K, uint8_t* packed, void* stream) {
+    if (q == nullptr || sf == nullptr || packed == nullptr) return DH_ERR_ARG;
+    if (N <= 0 || K <= 0 || N % 16 != 0 || K % 128 != 0) return DH_ERR_SHAPE;
+    if (static_cast<long long>(N) * K >= (1ll << 40)) return DH_ERR_SHAPE;
+    if (!aligned(q, 16) || !aligned(sf, 16) || !aligned(packed, 16)) return DH_ERR_ALIGN;
+    return cuda_status(dh::launch_nvfp4_pack(q, sf, N, K, packed, static_cast<cudaStream_t>(stream)));
 }
 
 size_t draft_head_workspace_bytes(const dh_head_t* hd, int M_max) {

@@ -53,15 +53,22 @@ struct Cfg {
     static constexpr int NW = NWIN <= 20 ? NWIN : 20;        // warps per CTA
     static constexpr int WPW = NWIN / NW;                    // windows per warp
     static constexpr int NT = MT <= 8 ? 1 : 2;               // n8 tiles of drafts
-    static constexpr bool BLOCKDIAG = (FMT == 1 && MT == 1);
-    static constexpr int BPE2 = FMT == 1 ? 1 : (FMT == 2 ? 2 : 4);  // bytes per 2 elements
+    static constexpr bool NV = (FMT == 1 || FMT == 4);       // NVFP4 (canonical or packed layout)
+    static constexpr bool PACKED = (FMT == 4);                // tile-major NVFP4 layout
+    static constexpr bool BLOCKDIAG = (NV && MT == 1);
+    static constexpr int BPE2 = NV ? 1 : (FMT == 2 ? 2 : 4);  // bytes per 2 elements
     static constexpr int RB = K * BPE2 / 2;                   // code bytes per head row
     static constexpr int WB = 128 * BPE2 / 2;                 // code bytes per row and window
     static constexpr int CPR = WB / 4 / 16;                   // 16-byte loads per row, window, thread
-    static constexpr int SFB = FMT == 1 ? K / 16 : 0;         // scale bytes per head row
-    static constexpr int TILE_REGS = WPW * (8 * CPR + (FMT == 1 ? 4 : 0));
+    static constexpr int SFB = NV ? K / 16 : 0;               // scale bytes per head row
+    static constexpr int WBLK = 16 * WB + 16 * 8;             // packed: bytes of one (tile, window) block
+    static constexpr int TILE_REGS = WPW * (8 * CPR + (NV ? 4 : 0));
     static constexpr int P = cmax(1, cmin(3, 48 / TILE_REGS));  // tiles of loads in flight
-    static constexpr int THREADS = NW * 32;
+    static constexpr bool SCALES = (FMT == 1);
+    static constexpr int THREADS = (NW + 1 + (SCALES ? 1 : 0)) * 32;  // + reducer (+ scale loader)
+    static constexpr int SS = 6;                                       // scale-tile ring slots
+    static constexpr int SCALE_TILE = 16 * SFB;                        // scale bytes of one tile
+    static constexpr int RS = (4 * NW * 16 * MT * 4 <= 40 * 1024) ? 4 : 2;  // partial-sum slots
     static_assert(NWIN % NW == 0, "windows must split evenly over warps");
     static_assert(K % 128 == 0, "K must be a multiple of 128");
 };
@@ -88,9 +95,10 @@ __device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
     return r;
 }
 
-// Bytes of the loads of one tile for one thread: per window, CPR 16-byte
-// pieces of row g and of row g+8, and (NVFP4) the window's 8 scale bytes of
-// both rows.
+// Code bytes of one tile held by one thread: per window, CPR 16-byte pieces of
+// row g and of row g+8, and for NVFP4 the window's 8 scale bytes of both rows
+// (loaded with the codes from the packed layout, or taken from the shared-
+// memory scale ring for the canonical layout).
 template <int FMT, int K, int MT>
 struct TileBuf {
     using C = Cfg<FMT, K, MT>;
@@ -99,23 +107,30 @@ struct TileBuf {
 };
 
 template <int FMT, int K, int MT>
-__device__ __forceinline__ void load_tile(TileBuf<FMT, K, MT>& b, const uint8_t* q, const uint8_t* sf, int tile,
-                                          int warp, int g, int t) {
+__device__ __forceinline__ void load_tile(TileBuf<FMT, K, MT>& b, const uint8_t* q, int tile, int warp, int g,
+                                          int t) {
     using C = Cfg<FMT, K, MT>;
 #pragma unroll
     for (int ww = 0; ww < C::WPW; ++ww) {
         const int w = warp + ww * C::NW;
+        if constexpr (C::PACKED) {
+            // block (tile, w): 16 rows x 64 code bytes, then 16 rows x 8 scale bytes
+            const uint8_t* blk = q + (static_cast<size_t>(tile) * C::NWIN + w) * C::WBLK;
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const size_t row = static_cast<size_t>(tile) * 16 + g + 8 * h;
-            const uint8_t* p = q + row * C::RB + w * C::WB + t * (C::WB / 4);
-#pragma unroll
-            for (int c = 0; c < C::CPR; ++c) b.c[ww][h][c] = ld_stream_v4(p + 16 * c);
-            if constexpr (FMT == 1) {
-                const uint8_t* ps = sf + row * C::SFB + 8 * w;
+            for (int h = 0; h < 2; ++h) {
+                b.c[ww][h][0] = ld_stream_v4(blk + (g + 8 * h) * 64 + 16 * t);
                 uint2 v;
-                asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(ps));
+                asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];"
+                             : "=r"(v.x), "=r"(v.y) : "l"(blk + 16 * 64 + (g + 8 * h) * 8));
                 b.s[ww][h] = v;
+            }
+        } else {
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const size_t row = static_cast<size_t>(tile) * 16 + g + 8 * h;
+                const uint8_t* p = q + row * C::RB + w * C::WB + t * (C::WB / 4);
+#pragma unroll
+                for (int c = 0; c < C::CPR; ++c) b.c[ww][h][c] = ld_stream_v4(p + 16 * c);
             }
         }
     }
@@ -144,17 +159,19 @@ __device__ __forceinline__ uint32_t word_of(const uint4 (&v)[CPR], int i) {
 template <int FMT, int K, int MT, bool LOGITS>
 __global__ void __launch_bounds__(Cfg<FMT, K, MT>::THREADS, 1) gemv_mma_kernel(const GemvArgs a) {
     using C = Cfg<FMT, K, MT>;
-    constexpr int NW = C::NW, WPW = C::WPW, NT = C::NT, P = C::P, KW = K / 2;
+    constexpr int NW = C::NW, WPW = C::WPW, NT = C::NT, P = C::P, KW = K / 2, RS = C::RS;
     constexpr int NTH = C::THREADS;
-    constexpr int NRED = 16 * MT;  // (row, draft) reducer slots of a tile
-    // tiles whose partials are reduced after one __syncthreads
-    constexpr int PS = (P > 1 && 2 * P * NW * 16 * MT * 4 <= 32 * 1024) ? P : 1;
-    __shared__ float s_part[2][PS][NW][16][MT];
-    __shared__ unsigned long long s_best[PS * NRED];
-    __shared__ float s_red[NW][MT];
+    constexpr int NRED = 16 * MT;  // (row, draft) results of a tile
+    __shared__ float s_part[RS][NW][16][MT];
+    __shared__ __align__(8) uint64_t full_p[RS];
+    __shared__ __align__(8) uint64_t empty_p[RS];
+    __shared__ __align__(8) uint64_t full_s[C::SS];
+    __shared__ __align__(8) uint64_t empty_s[C::SS];
+    extern __shared__ __align__(16) uint8_t s_scales[];  // [SS][16 rows][K/16] (NVFP4)
+    __shared__ unsigned long long s_best[NRED];
     __shared__ float s_mul[MT];
-    __shared__ int s_exp[MT];
     __shared__ unsigned long long s_cta[MT];
+    __shared__ int s_abort;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int g = lane >> 2, t = lane & 3;
     const int n_tiles = a.N / 16;
@@ -162,254 +179,339 @@ __global__ void __launch_bounds__(Cfg<FMT, K, MT>::THREADS, 1) gemv_mma_kernel(c
                              ? (n_tiles - 1 - static_cast<int>(blockIdx.x)) / static_cast<int>(gridDim.x) + 1
                              : 0;
     const uint8_t* q = static_cast<const uint8_t*>(a.q);
+    volatile int* abort_flag = &s_abort;
 
-    // Issue the first P tiles' loads before anything else.
+    // Issue the first P tiles' loads before anything else (compute warps).
     TileBuf<FMT, K, MT> buf[P];
+    if (warp < NW) {
 #pragma unroll
-    for (int p = 0; p < P; ++p)
-        if (p < my_tiles) load_tile<FMT, K, MT>(buf[p], q, a.sf, blockIdx.x + p * gridDim.x, warp, g, t);
-
-    // Per-draft power-of-two prescale of h so that it converts to f16 exactly
-    // (BF16 heads use h as it is).
-    const uint32_t* h32 = reinterpret_cast<const uint32_t*>(a.h);
-    {
-        float am[MT];
-#pragma unroll
-        for (int m = 0; m < MT; ++m) am[m] = 0.0f;
-        for (int i = tid; i < KW; i += NTH) {
-#pragma unroll
-            for (int m = 0; m < MT; ++m)
-                if (m < a.M) {
-                    const uint32_t w = __ldg(h32 + m * KW + i);
-                    am[m] = fmaxf(am[m], fmaxf(fabsf(bf16_lo(w)), fabsf(bf16_hi(w))));
-                }
-        }
-#pragma unroll
-        for (int m = 0; m < MT; ++m) {
-            float v = am[m];
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
-            if (lane == 0) s_red[warp][m] = v;
-        }
-        for (int i = tid; i < PS * NRED; i += NTH) s_best[i] = 0ull;
-        __syncthreads();
-        if (tid < MT) {
-            float v = 0.0f;
-            for (int w = 0; w < NW; ++w) v = fmaxf(v, s_red[w][tid]);
-            const int e = (FMT == 3) ? 0 : f16_prescale_exponent(v);
-            s_exp[tid] = e;
-            s_mul[tid] = (FMT == 3 ? 1.0f : __ldg(a.scale)) * exp2i(-e);
-        }
-        __syncthreads();
+        for (int p = 0; p < P; ++p)
+            if (p < my_tiles) load_tile<FMT, K, MT>(buf[p], q, blockIdx.x + p * gridDim.x, warp, g, t);
     }
+    if (tid == 0) {
+        for (int r = 0; r < RS; ++r) {
+            mbar_init(&full_p[r], NW);
+            mbar_init(&empty_p[r], 1);
+        }
+        for (int r = 0; r < C::SS; ++r) {
+            mbar_init(&full_s[r], 1);
+            mbar_init(&empty_s[r], NW);
+        }
+        s_abort = 0;
+        mbar_init_fence();
+    }
+    if (tid < MT) s_mul[tid] = (FMT == 3) ? 1.0f : 0.0f;
+    // Programmatic dependent launch: everything above only touched the head,
+    // which the preceding kernel in the stream does not write; h, the
+    // workspace and the outputs are used only after its completion.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;");
+    if (tid < MT && FMT != 3) s_mul[tid] = __ldg(a.scale);
+    __syncthreads();
+    const uint32_t* h32 = reinterpret_cast<const uint32_t*>(a.h);
 
-    // This thread's h words (B fragments), per window and n8 tile: word j holds
-    // h[d][k0 + 2j], h[d][k0 + 2j + 1] with k0 = 128 w + 32 t and d = g + 8 nt
-    // (d = 0 in the block-diagonal case, where the columns are blocks).
-    uint32_t hb[WPW][NT][16];
-#pragma unroll
-    for (int ww = 0; ww < WPW; ++ww)
+    if (warp == NW + 1) {
+        // -------------------------------------------------- scale loader ----
+        // The 16 x K/16 scale bytes of a tile are contiguous: one 1-D bulk copy
+        // per tile into a ring of SS slots (their per-row 8-byte pieces would
+        // otherwise cost one L2 request per row and window).
+        if constexpr (C::SCALES) {
+            if (lane == 0) {
+                const uint64_t pol = policy_evict_first();
+                int issued = 0;
+                for (int i = 0; i < my_tiles; ++i) {
+                    const int slot = i % C::SS;
+                    if (i >= C::SS && !mbar_wait(&empty_s[slot], ((i / C::SS) - 1) & 1)) {
+                        atomicOr(&a.ws->error, kDevErrTimeout);
+                        *abort_flag = 1;
+                    }
+                    if (*abort_flag) break;
+                    const int tile = static_cast<int>(blockIdx.x) + i * static_cast<int>(gridDim.x);
+                    mbar_arrive_expect_tx(&full_s[slot], C::SCALE_TILE);
+                    bulk_g2s(s_scales + slot * C::SCALE_TILE, a.sf + static_cast<size_t>(tile) * C::SCALE_TILE,
+                             C::SCALE_TILE, &full_s[slot], pol);
+                    ++issued;
+                }
+                if (*abort_flag) {  // let the copies already issued land before the CTA exits
+                    for (int i = issued > C::SS ? issued - C::SS : 0; i < issued; ++i)
+                        (void)mbar_wait(&full_s[i % C::SS], (i / C::SS) & 1);
+                }
+            }
+            __syncwarp();
+        }
+    } else if (warp == NW) {
+        // ------------------------------------------------------- reducer ----
+        // Sums the NW partials of each tile in a fixed order and keeps the
+        // best key per (row, draft), or writes the logits; never blocks the
+        // compute warps except when it falls RS tiles behind.
+        for (int r = lane; r < NRED; r += 32) s_best[r] = 0ull;
+        for (int i = 0; i < my_tiles; ++i) {
+            const int slot = i % RS;
+            if (!*abort_flag && !mbar_wait(&full_p[slot], (i / RS) & 1)) {
+                atomicOr(&a.ws->error, kDevErrTimeout);
+                *abort_flag = 1;
+            }
+            const int tile = static_cast<int>(blockIdx.x) + i * static_cast<int>(gridDim.x);
+            for (int r = lane; r < NRED; r += 32) {
+                const int row_t = r / MT, m = r % MT;
+                float v = 0.0f;
+#pragma unroll 4
+                for (int w = 0; w < NW; ++w) v += s_part[slot][w][row_t][m];
+                const int row = tile * 16 + row_t;
+                if (m < a.M && row < a.n_kept) {
+                    const float y = v * s_mul[m];
+                    if constexpr (LOGITS) {
+                        scatter_one(a, m, row, y);
+                    } else {
+                        const unsigned long long k = argmax_key(ordered_key(y), static_cast<uint32_t>(row));
+                        if (k > s_best[r]) s_best[r] = k;
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty_p[slot]);
+        }
+    } else {
+        // -------------------------------------------------- compute warps ----
+        // This thread's h words (B fragments), per window and n8 tile: word j
+        // holds h[d][k0 + 2j], h[d][k0 + 2j + 1] with k0 = 128 w + 32 t and
+        // d = g + 8 nt (d = 0 in the block-diagonal case, where the columns are
+        // blocks). For the f16 MMAs, h is scaled by 2^e with e chosen per warp
+        // and draft from the largest |h| over this warp's windows, so that every
+        // BF16 value converts to f16 exactly; the warp's partial logits are
+        // scaled back by 2^-e before they leave it.
+        uint32_t hb[WPW][NT][16];
+        float unscale[NT][2];  // 2^-e of the drafts of this thread's D columns
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
-            // the draft of B column g (one draft only in the block-diagonal case)
             const int d = C::BLOCKDIAG ? 0 : g + 8 * nt;
-            const int k0 = 128 * (warp + ww * NW) + 32 * t;
-            const float sc = d < a.M ? exp2i(s_exp[d < MT ? d : 0]) : 0.0f;
+            const bool live = d < a.M;
+            float am = 0.0f;
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                uint32_t w = 0u;
-                if (d < a.M) w = __ldg(h32 + d * KW + k0 / 2 + j);
-                if constexpr (FMT == 3) {
+            for (int ww = 0; ww < WPW; ++ww) {
+                const int k0 = 128 * (warp + ww * NW) + 32 * t;
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const uint32_t w = live ? __ldg(h32 + d * KW + k0 / 2 + j) : 0u;
                     hb[ww][nt][j] = w;
-                } else {
-                    __half2 v = __floats2half2_rn(bf16_lo(w) * sc, bf16_hi(w) * sc);
-                    hb[ww][nt][j] = *reinterpret_cast<uint32_t*>(&v);
+                    am = fmaxf(am, fmaxf(fabsf(bf16_lo(w)), fabsf(bf16_hi(w))));
                 }
+            }
+            // the 4 threads of a group (same g, so same draft) cover the window
+            am = fmaxf(am, __shfl_xor_sync(0xFFFFFFFFu, am, 1));
+            am = fmaxf(am, __shfl_xor_sync(0xFFFFFFFFu, am, 2));
+            if constexpr (C::BLOCKDIAG) {
+#pragma unroll
+                for (int o = 4; o < 32; o <<= 1) am = fmaxf(am, __shfl_xor_sync(0xFFFFFFFFu, am, o));
+            }
+            const int e = (FMT == 3) ? 0 : f16_prescale_exponent(am);
+            const float sc = exp2i(e);
+            const float inv = exp2i(-e);
+            if constexpr (FMT != 3) {
+#pragma unroll
+                for (int ww = 0; ww < WPW; ++ww)
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const uint32_t w = hb[ww][nt][j];
+                        __half2 v = __floats2half2_rn(bf16_lo(w) * sc, bf16_hi(w) * sc);
+                        hb[ww][nt][j] = *reinterpret_cast<uint32_t*>(&v);
+                    }
+            }
+            if constexpr (C::BLOCKDIAG) {
+                unscale[nt][0] = inv;
+                unscale[nt][1] = inv;
+#pragma unroll
+                for (int ww = 0; ww < WPW; ++ww)
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        // b0 of MMA i is nonzero only for t == g (pair p = t), b1 only
+                        // for t + 4 == g (pair p = t + 4)
+                        const bool keep = (j < 8) ? (t == g) : (t + 4 == g);
+                        hb[ww][nt][j] = keep ? hb[ww][nt][j] : 0u;
+                    }
+            } else {
+                // D columns 2t, 2t+1 hold drafts 8 nt + 2t (+1), whose scale lives
+                // in the lanes of group g = 2t (+1)
+                unscale[nt][0] = __shfl_sync(0xFFFFFFFFu, inv, 4 * (2 * t));
+                unscale[nt][1] = __shfl_sync(0xFFFFFFFFu, inv, 4 * (2 * t + 1));
             }
         }
-    if constexpr (C::BLOCKDIAG) {
-        // b0 of MMA i is nonzero only for t == g (pair p = t), b1 only for
-        // t + 4 == g (pair p = t + 4); keep word i of each half or zero.
-#pragma unroll
-        for (int ww = 0; ww < WPW; ++ww)
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                const bool keep = (j < 8) ? (t == g) : (t + 4 == g);
-                hb[ww][0][j] = keep ? hb[ww][0][j] : 0u;
-            }
-    }
+        // Blocks of this thread's D columns 2t, 2t+1 under pi (block-diagonal case).
+        const int blk0 = (2 * t < 4) ? 4 * t : 4 * t - 7;
+        const int blk1 = blk0 + 2;
 
-    // Blocks of this thread's D columns 2t, 2t+1 under pi (block-diagonal case).
-    const int blk0 = (2 * t < 4) ? 4 * t : 4 * t - 7;
-    const int blk1 = blk0 + 2;
-
-    const float* smul = s_mul;
-    for (int it = 0; it < my_tiles; it += P) {
+        for (int it = 0; it < my_tiles; it += P) {
 #pragma unroll
-        for (int p = 0; p < P; ++p) {
-            const int ti = it + p;
-            if (ti >= my_tiles) break;
-            TileBuf<FMT, K, MT>& b = buf[p];
-            const int par = (PS == 1 ? ti : it / P) & 1;
-            const int ps = PS == 1 ? 0 : p;
-            if constexpr (C::BLOCKDIAG) {
-                float y0 = 0.0f, y1 = 0.0f;  // partial logits of rows g, g+8
-#pragma unroll
-                for (int ww = 0; ww < WPW; ++ww) {
-                    float d[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-                    // MMA i takes byte i (block 2t) and byte 8+i (block 2t+1) of each row:
-                    // words (0, 2) feed i < 4, words (1, 3) feed i >= 4.
-#pragma unroll
-                    for (int half = 0; half < 2; ++half) {
-                        uint32_t fg0[4], fg1[4], fh0[4], fh1[4];
-                        const uint4& cg = b.c[ww][0][0];
-                        const uint4& ch = b.c[ww][1][0];
-                        e2m1x8_to_f16x2(half ? cg.y : cg.x, fg0);
-                        e2m1x8_to_f16x2(half ? cg.w : cg.z, fg1);
-                        e2m1x8_to_f16x2(half ? ch.y : ch.x, fh0);
-                        e2m1x8_to_f16x2(half ? ch.w : ch.z, fh1);
-#pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-                            const int i = 4 * half + j;
-                            mma_f16(d, fg0[j], fh0[j], fg1[j], fh1[j], hb[ww][0][i], hb[ww][0][8 + i]);
-                        }
+            for (int p = 0; p < P; ++p) {
+                const int ti = it + p;
+                if (ti >= my_tiles) break;
+                TileBuf<FMT, K, MT>& b = buf[p];
+                const int slot = ti % RS;
+                if constexpr (C::SCALES) {
+                    const int ss = ti % C::SS;
+                    if (!*abort_flag && !mbar_wait(&full_s[ss], (ti / C::SS) & 1)) {
+                        atomicOr(&a.ws->error, kDevErrTimeout);
+                        *abort_flag = 1;
                     }
-                    // scales of blocks blk0, blk1 of rows g, g+8 (bytes of the window's 8)
-                    const uint32_t sel = static_cast<uint32_t>(blk0) | (static_cast<uint32_t>(blk1) << 4);
-                    uint32_t s01g, s01h;
-                    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(s01g) : "r"(b.s[ww][0].x), "r"(b.s[ww][0].y), "r"(sel));
-                    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(s01h) : "r"(b.s[ww][1].x), "r"(b.s[ww][1].y), "r"(sel));
-                    const uint32_t fg = e4m3x2_to_f16x2(s01g), fh = e4m3x2_to_f16x2(s01h);
-                    y0 = fmaf(d[0], f16lo(fg), y0);
-                    y0 = fmaf(d[1], f16hi(fg), y0);
-                    y1 = fmaf(d[2], f16lo(fh), y1);
-                    y1 = fmaf(d[3], f16hi(fh), y1);
-                }
-                y0 += __shfl_xor_sync(0xFFFFFFFFu, y0, 1);
-                y0 += __shfl_xor_sync(0xFFFFFFFFu, y0, 2);
-                y1 += __shfl_xor_sync(0xFFFFFFFFu, y1, 1);
-                y1 += __shfl_xor_sync(0xFFFFFFFFu, y1, 2);
-                if (t == 0) {
-                    s_part[par][ps][warp][g][0] = y0;
-                    s_part[par][ps][warp][g + 8][0] = y1;
-                }
-            } else {
-                float d[NT][4];
+                    const uint8_t* st = s_scales + ss * C::SCALE_TILE;
 #pragma unroll
-                for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) d[nt][c] = 0.0f;
-#pragma unroll
-                for (int ww = 0; ww < WPW; ++ww) {
-                    uint32_t sg0 = 0u, sg1 = 0u, sh0 = 0u, sh1 = 0u;  // (s, s) f16x2 per row and block
-                    if constexpr (FMT == 1) {
-                        // blocks 2t, 2t+1 of the window: bytes 2t, 2t+1 of its 8 scale bytes
-                        const uint32_t sel = static_cast<uint32_t>(2 * t) | (static_cast<uint32_t>(2 * t + 1) << 4);
-                        uint32_t s2g, s2h;
-                        asm("prmt.b32 %0, %1, %2, %3;" : "=r"(s2g) : "r"(b.s[ww][0].x), "r"(b.s[ww][0].y), "r"(sel));
-                        asm("prmt.b32 %0, %1, %2, %3;" : "=r"(s2h) : "r"(b.s[ww][1].x), "r"(b.s[ww][1].y), "r"(sel));
-                        const uint32_t fg = e4m3x2_to_f16x2(s2g), fh = e4m3x2_to_f16x2(s2h);
-                        asm("prmt.b32 %0, %1, 0, 0x1010;" : "=r"(sg0) : "r"(fg));
-                        asm("prmt.b32 %0, %1, 0, 0x3232;" : "=r"(sg1) : "r"(fg));
-                        asm("prmt.b32 %0, %1, 0, 0x1010;" : "=r"(sh0) : "r"(fh));
-                        asm("prmt.b32 %0, %1, 0, 0x3232;" : "=r"(sh1) : "r"(fh));
+                    for (int ww = 0; ww < WPW; ++ww) {
+                        const int w = warp + ww * NW;
+                        b.s[ww][0] = *reinterpret_cast<const uint2*>(st + g * C::SFB + 8 * w);
+                        b.s[ww][1] = *reinterpret_cast<const uint2*>(st + (g + 8) * C::SFB + 8 * w);
                     }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&empty_s[ss]);
+                }
+                float out[NT][4];  // block-diagonal: out[0][0..1] = rows g, g+8
+                if constexpr (C::BLOCKDIAG) {
+                    float y0 = 0.0f, y1 = 0.0f;
 #pragma unroll
-                    for (int q4 = 0; q4 < 4; ++q4) {
-                        // MMAs i = 2 q4, 2 q4 + 1: NVFP4 codes 4i..4i+3 are bytes 2i, 2i+1,
-                        // i.e. word q4 of the row's 16 bytes; blocks: q4 < 2 -> 2t, else 2t+1
-                        uint32_t fg[4], fh[4];
-                        if constexpr (FMT == 1) {
+                    for (int ww = 0; ww < WPW; ++ww) {
+                        float d[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+                        // MMA i takes byte i (block 2t) and byte 8+i (block 2t+1) of each
+                        // row: words (0, 2) feed i < 4, words (1, 3) feed i >= 4.
+#pragma unroll
+                        for (int half = 0; half < 2; ++half) {
+                            uint32_t fg0[4], fg1[4], fh0[4], fh1[4];
                             const uint4& cg = b.c[ww][0][0];
                             const uint4& ch = b.c[ww][1][0];
-                            const uint32_t wg = q4 == 0 ? cg.x : (q4 == 1 ? cg.y : (q4 == 2 ? cg.z : cg.w));
-                            const uint32_t wh = q4 == 0 ? ch.x : (q4 == 1 ? ch.y : (q4 == 2 ? ch.z : ch.w));
-                            e2m1x8_to_f16x2(wg, fg);
-                            e2m1x8_to_f16x2(wh, fh);
-                            const uint32_t sg = q4 < 2 ? sg0 : sg1, sh = q4 < 2 ? sh0 : sh1;
+                            e2m1x8_to_f16x2(half ? cg.y : cg.x, fg0);
+                            e2m1x8_to_f16x2(half ? cg.w : cg.z, fg1);
+                            e2m1x8_to_f16x2(half ? ch.y : ch.x, fh0);
+                            e2m1x8_to_f16x2(half ? ch.w : ch.z, fh1);
 #pragma unroll
                             for (int j = 0; j < 4; ++j) {
-                                fg[j] = hmul2(fg[j], sg);
-                                fh[j] = hmul2(fh[j], sh);
+                                const int i = 4 * half + j;
+                                mma_f16(d, fg0[j], fh0[j], fg1[j], fh1[j], hb[ww][0][i], hb[ww][0][8 + i]);
                             }
                         }
+                        // scales of blocks blk0, blk1 of rows g, g+8 (bytes of the window's 8)
+                        const uint32_t sel = static_cast<uint32_t>(blk0) | (static_cast<uint32_t>(blk1) << 4);
+                        uint32_t s01g, s01h;
+                        asm("prmt.b32 %0, %1, %2, %3;" : "=r"(s01g) : "r"(b.s[ww][0].x), "r"(b.s[ww][0].y), "r"(sel));
+                        asm("prmt.b32 %0, %1, %2, %3;" : "=r"(s01h) : "r"(b.s[ww][1].x), "r"(b.s[ww][1].y), "r"(sel));
+                        const uint32_t fg = e4m3x2_to_f16x2(s01g), fh = e4m3x2_to_f16x2(s01h);
+                        y0 = fmaf(d[0], f16lo(fg), y0);
+                        y0 = fmaf(d[1], f16hi(fg), y0);
+                        y1 = fmaf(d[2], f16lo(fh), y1);
+                        y1 = fmaf(d[3], f16hi(fh), y1);
+                    }
+                    y0 += __shfl_xor_sync(0xFFFFFFFFu, y0, 1);
+                    y0 += __shfl_xor_sync(0xFFFFFFFFu, y0, 2);
+                    y1 += __shfl_xor_sync(0xFFFFFFFFu, y1, 1);
+                    y1 += __shfl_xor_sync(0xFFFFFFFFu, y1, 2);
+                    out[0][0] = y0;
+                    out[0][1] = y1;
+                } else {
 #pragma unroll
-                        for (int jj = 0; jj < 2; ++jj) {
-                            const int i = 2 * q4 + jj;
-                            uint32_t a0, a1, a2, a3;
-                            if constexpr (FMT == 1) {
-                                a0 = fg[2 * jj];
-                                a1 = fh[2 * jj];
-                                a2 = fg[2 * jj + 1];
-                                a3 = fh[2 * jj + 1];
-                            } else if constexpr (FMT == 2) {
-                                const uint32_t wg = word_of<C::CPR>(b.c[ww][0], i), wh = word_of<C::CPR>(b.c[ww][1], i);
-                                a0 = e4m3x2_to_f16x2(wg & 0xFFFFu);
-                                a1 = e4m3x2_to_f16x2(wh & 0xFFFFu);
-                                a2 = e4m3x2_to_f16x2(wg >> 16);
-                                a3 = e4m3x2_to_f16x2(wh >> 16);
-                            } else {
-                                a0 = word_of<C::CPR>(b.c[ww][0], 2 * i);
-                                a1 = word_of<C::CPR>(b.c[ww][1], 2 * i);
-                                a2 = word_of<C::CPR>(b.c[ww][0], 2 * i + 1);
-                                a3 = word_of<C::CPR>(b.c[ww][1], 2 * i + 1);
+                    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) out[nt][c] = 0.0f;
+#pragma unroll
+                    for (int ww = 0; ww < WPW; ++ww) {
+                        uint32_t sg0 = 0u, sg1 = 0u, sh0 = 0u, sh1 = 0u;  // (s, s) f16x2 per row and block
+                        if constexpr (C::NV) {
+                            // blocks 2t, 2t+1 of the window: bytes 2t, 2t+1 of its 8 scale bytes
+                            const uint32_t sel = static_cast<uint32_t>(2 * t) | (static_cast<uint32_t>(2 * t + 1) << 4);
+                            uint32_t s2g, s2h;
+                            asm("prmt.b32 %0, %1, %2, %3;" : "=r"(s2g) : "r"(b.s[ww][0].x), "r"(b.s[ww][0].y), "r"(sel));
+                            asm("prmt.b32 %0, %1, %2, %3;" : "=r"(s2h) : "r"(b.s[ww][1].x), "r"(b.s[ww][1].y), "r"(sel));
+                            const uint32_t fg = e4m3x2_to_f16x2(s2g), fh = e4m3x2_to_f16x2(s2h);
+                            asm("prmt.b32 %0, %1, 0, 0x1010;" : "=r"(sg0) : "r"(fg));
+                            asm("prmt.b32 %0, %1, 0, 0x3232;" : "=r"(sg1) : "r"(fg));
+                            asm("prmt.b32 %0, %1, 0, 0x1010;" : "=r"(sh0) : "r"(fh));
+                            asm("prmt.b32 %0, %1, 0, 0x3232;" : "=r"(sh1) : "r"(fh));
+                        }
+#pragma unroll
+                        for (int q4 = 0; q4 < 4; ++q4) {
+                            // MMAs i = 2 q4, 2 q4 + 1: NVFP4 codes 4i..4i+3 are bytes 2i, 2i+1,
+                            // i.e. word q4 of the row's 16 bytes; blocks: q4 < 2 -> 2t, else 2t+1
+                            uint32_t fg[4], fh[4];
+                            if constexpr (C::NV) {
+                                const uint4& cg = b.c[ww][0][0];
+                                const uint4& ch = b.c[ww][1][0];
+                                const uint32_t wg = q4 == 0 ? cg.x : (q4 == 1 ? cg.y : (q4 == 2 ? cg.z : cg.w));
+                                const uint32_t wh = q4 == 0 ? ch.x : (q4 == 1 ? ch.y : (q4 == 2 ? ch.z : ch.w));
+                                e2m1x8_to_f16x2(wg, fg);
+                                e2m1x8_to_f16x2(wh, fh);
+                                const uint32_t sg = q4 < 2 ? sg0 : sg1, sh = q4 < 2 ? sh0 : sh1;
+#pragma unroll
+                                for (int j = 0; j < 4; ++j) {
+                                    fg[j] = hmul2(fg[j], sg);
+                                    fh[j] = hmul2(fh[j], sh);
+                                }
                             }
 #pragma unroll
-                            for (int nt = 0; nt < NT; ++nt) {
-                                if constexpr (FMT == 3)
-                                    mma_bf16(d[nt], a0, a1, a2, a3, hb[ww][nt][2 * i], hb[ww][nt][2 * i + 1]);
-                                else
-                                    mma_f16(d[nt], a0, a1, a2, a3, hb[ww][nt][2 * i], hb[ww][nt][2 * i + 1]);
+                            for (int jj = 0; jj < 2; ++jj) {
+                                const int i = 2 * q4 + jj;
+                                uint32_t a0, a1, a2, a3;
+                                if constexpr (C::NV) {
+                                    a0 = fg[2 * jj];
+                                    a1 = fh[2 * jj];
+                                    a2 = fg[2 * jj + 1];
+                                    a3 = fh[2 * jj + 1];
+                                } else if constexpr (FMT == 2) {
+                                    const uint32_t wg = word_of<C::CPR>(b.c[ww][0], i), wh = word_of<C::CPR>(b.c[ww][1], i);
+                                    a0 = e4m3x2_to_f16x2(wg & 0xFFFFu);
+                                    a1 = e4m3x2_to_f16x2(wh & 0xFFFFu);
+                                    a2 = e4m3x2_to_f16x2(wg >> 16);
+                                    a3 = e4m3x2_to_f16x2(wh >> 16);
+                                } else {
+                                    a0 = word_of<C::CPR>(b.c[ww][0], 2 * i);
+                                    a1 = word_of<C::CPR>(b.c[ww][1], 2 * i);
+                                    a2 = word_of<C::CPR>(b.c[ww][0], 2 * i + 1);
+                                    a3 = word_of<C::CPR>(b.c[ww][1], 2 * i + 1);
+                                }
+#pragma unroll
+                                for (int nt = 0; nt < NT; ++nt) {
+                                    if constexpr (FMT == 3)
+                                        mma_bf16(out[nt], a0, a1, a2, a3, hb[ww][nt][2 * i], hb[ww][nt][2 * i + 1]);
+                                    else
+                                        mma_f16(out[nt], a0, a1, a2, a3, hb[ww][nt][2 * i], hb[ww][nt][2 * i + 1]);
+                                }
                             }
                         }
                     }
                 }
-#pragma unroll
-                for (int nt = 0; nt < NT; ++nt) {
-                    const int m0 = 8 * nt + 2 * t;
-                    if (m0 < MT) {
-                        s_part[par][ps][warp][g][m0] = d[nt][0];
-                        s_part[par][ps][warp][g + 8][m0] = d[nt][2];
-                    }
-                    if (m0 + 1 < MT) {
-                        s_part[par][ps][warp][g][m0 + 1] = d[nt][1];
-                        s_part[par][ps][warp][g + 8][m0 + 1] = d[nt][3];
-                    }
+                // loads of the tile P steps ahead go into the buffer just consumed
+                const int tn = ti + P;
+                if (tn < my_tiles) load_tile<FMT, K, MT>(buf[p], q, blockIdx.x + tn * gridDim.x, warp, g, t);
+                // hand the partials to the reducer (wait for the slot to be free first)
+                if (ti >= RS && !*abort_flag && !mbar_wait(&empty_p[slot], ((ti / RS) - 1) & 1)) {
+                    atomicOr(&a.ws->error, kDevErrTimeout);
+                    *abort_flag = 1;
                 }
-            }
-            // loads of the tile P steps ahead go into the buffer just consumed
-            const int tn = ti + P;
-            if (tn < my_tiles) load_tile<FMT, K, MT>(buf[p], q, a.sf, blockIdx.x + tn * gridDim.x, warp, g, t);
-            if (PS == 1 || p == P - 1 || ti == my_tiles - 1) {
-                __syncthreads();
-                for (int r = tid; r < PS * NRED; r += NTH) {
-                    const int pr = r / NRED, rem = r % NRED;
-                    const int row_t = rem / MT, m = rem % MT;
-                    const int tr = PS == 1 ? ti : it + pr;
-                    if (tr > ti) continue;
-                    float v = 0.0f;
-#pragma unroll 4
-                    for (int w = 0; w < NW; ++w) v += s_part[par][pr][w][row_t][m];
-                    const int row = (blockIdx.x + tr * gridDim.x) * 16 + row_t;
-                    if (m < a.M && row < a.n_kept) {
-                        const float y = v * smul[m];
-                        if constexpr (LOGITS) {
-                            scatter_one(a, m, row, y);
-                        } else {
-                            const unsigned long long k = argmax_key(ordered_key(y), static_cast<uint32_t>(row));
-                            if (k > s_best[r]) s_best[r] = k;
+                if constexpr (C::BLOCKDIAG) {
+                    if (t == 0) {
+                        s_part[slot][warp][g][0] = out[0][0] * unscale[0][0];
+                        s_part[slot][warp][g + 8][0] = out[0][1] * unscale[0][0];
+                    }
+                } else {
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt) {
+                        const int m0 = 8 * nt + 2 * t;
+                        if (m0 < MT) {
+                            s_part[slot][warp][g][m0] = out[nt][0] * unscale[nt][0];
+                            s_part[slot][warp][g + 8][m0] = out[nt][2] * unscale[nt][0];
+                        }
+                        if (m0 + 1 < MT) {
+                            s_part[slot][warp][g][m0 + 1] = out[nt][1] * unscale[nt][1];
+                            s_part[slot][warp][g + 8][m0 + 1] = out[nt][3] * unscale[nt][1];
                         }
                     }
                 }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&full_p[slot]);
             }
         }
     }
+    __syncthreads();
     if constexpr (!LOGITS) {
-        __syncthreads();
         if (tid < MT) {
             unsigned long long k = 0ull;
-            for (int r = tid; r < PS * NRED; r += MT) {
-                const unsigned long long v = s_best[r];
+            for (int row_t = 0; row_t < 16; ++row_t) {
+                const unsigned long long v = s_best[row_t * MT + tid];
                 k = v > k ? v : k;
             }
             s_cta[tid] = k;
@@ -425,17 +527,35 @@ inline cudaError_t launch_mma(const GemvArgs& a, cudaStream_t s) {
     auto kern = gemv_mma_kernel<FMT, K, MT, LOGITS>;
     const int sms = sm_count();
     if (sms <= 0) return cudaErrorInvalidDevice;
-    static int occ = 0;
-    if (occ == 0) {
-        int o = 0;
-        const cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, kern, C::THREADS, 0);
+    const size_t smem = C::SCALES ? static_cast<size_t>(C::SS) * C::SCALE_TILE : 0;
+    static int occ[64] = {0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (occ[dev] == 0) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
         if (e != cudaSuccess) return e;
-        occ = o > 0 ? o : 1;
+        int o = 0;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, kern, C::THREADS, smem);
+        if (e != cudaSuccess) return e;
+        occ[dev] = o > 0 ? o : 1;
     }
     const int n_tiles = a.N / 16;
-    int blocks = sms * occ;
+    int blocks = sms * occ[dev];
     if (blocks > n_tiles) blocks = n_tiles;
-    kern<<<blocks, C::THREADS, 0, s>>>(a);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(blocks);
+    cfg.blockDim = dim3(C::THREADS);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, kern, a);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 

@@ -1,0 +1,16 @@
+// Draft-step kernels for the NVFP4 head in the packed tile-major layout
+// (instantiations of dh_gemv_mma.cuh).
+#include "dh_gemv_mma.cuh"
+
+namespace dh {
+
+cudaError_t launch_gemv_nvfp4_packed(const GemvArgs& a, cudaStream_t s) {
+    switch (a.K) {
+        case 256: return mma::launch_mma_k<4, 256>(a, s);
+        case 2560: return mma::launch_mma_k<4, 2560>(a, s);
+        case 5120: return mma::launch_mma_k<4, 5120>(a, s);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace dh

@@ -35,6 +35,10 @@ bool gemv_supported(int fmt, int K);
 // cudaError_t of the launch.
 cudaError_t launch_gemv(const GemvArgs& a, cudaStream_t s);
 
+// Repack a canonical NVFP4 head (q [N][K/2], sf [N][K/16]) into the
+// tile-major layout of DH_FMT_NVFP4_PACKED (N % 16 == 0, K % 128 == 0).
+cudaError_t launch_nvfp4_pack(const uint8_t* q, const uint8_t* sf, int N, int K, uint8_t* out, cudaStream_t s);
+
 // Fill out[0..count) with -inf.
 cudaError_t launch_fill_neg_inf(float* out, size_t count, cudaStream_t s);
 
@@ -47,5 +51,10 @@ cudaError_t launch_fp8_quantize(const uint16_t* W, int V, int K, const int32_t* 
 
 // Number of SMs of the current device (cached per device).
 int sm_count();
+
+// Encode a 2-D TMA tensor map (128 bytes at map128, 64-byte aligned) over a
+// row-major byte matrix [rows][row_bytes], boxes of box_rows x box_bytes.
+cudaError_t make_byte_tmap(void* map128, const void* base, uint64_t row_bytes, uint64_t rows,
+                           uint32_t box_bytes, uint32_t box_rows);
 
 }  // namespace dh

@@ -44,12 +44,13 @@ extern "C" int draft_head_top_tokens_static(const dh_head_t* hd, const void* h, 
     if (hd == nullptr || h == nullptr || ids == nullptr) return DH_ERR_ARG;
     if (M < 1 || M > DH_MAX_M) return DH_ERR_SHAPE;  // the scratch holds keys for 16 drafts
     if (hd->q == nullptr) return DH_ERR_ARG;
-    if (hd->fmt != DH_FMT_NVFP4 && hd->fmt != DH_FMT_FP8 && hd->fmt != DH_FMT_BF16) return DH_ERR_ARG;
+    if (hd->fmt != DH_FMT_NVFP4 && hd->fmt != DH_FMT_FP8 && hd->fmt != DH_FMT_BF16 && hd->fmt != DH_FMT_NVFP4_PACKED)
+        return DH_ERR_ARG;
     if (hd->V <= 0 || hd->N <= 0 || hd->n_kept < 1 || hd->n_kept > hd->N || hd->N % 64 != 0)
         return DH_ERR_SHAPE;
     if (!dh::gemv_supported(hd->fmt, hd->K)) return DH_ERR_SHAPE;
     if (hd->fmt == DH_FMT_NVFP4 && (hd->sf == nullptr || hd->scale == nullptr)) return DH_ERR_ARG;
-    if (hd->fmt == DH_FMT_FP8 && hd->scale == nullptr) return DH_ERR_ARG;
+    if ((hd->fmt == DH_FMT_FP8 || hd->fmt == DH_FMT_NVFP4_PACKED) && hd->scale == nullptr) return DH_ERR_ARG;
     if (hd->idx == nullptr && (hd->fmt != DH_FMT_BF16 || hd->n_kept != hd->N || hd->N > hd->V))
         return DH_ERR_ARG;
     const uintptr_t al16 = reinterpret_cast<uintptr_t>(hd->q) | reinterpret_cast<uintptr_t>(h) |

@@ -15,7 +15,7 @@ import nvfp4_draft_head_gb300 as dh
 import oracle
 import synthetic as syn
 from parity_util import Workload, check_argmax_rows, check_logits, ids_to_rows, plant_near_ties
-from test_parity_gpu import dev, dev_bf16, run_step
+from test_parity_gpu import dev, dev_bf16, pack_reference, run_step
 
 pytestmark = pytest.mark.gpu
 
@@ -45,28 +45,39 @@ def qwen64k(W_full):
 
 
 @pytest.fixture(scope="module")
-def head64k(qwen64k, W_dev):
+def canon64k(qwen64k, W_dev):
     idx = dev(qwen64k.idx)
     q, sf, g = dh.nvfp4_quantize_rows(W_dev, idx)
     return dh.DraftHead(dh.DH_FMT_NVFP4, qwen64k.V, q, idx, qwen64k.n_kept, sf=sf, scale=g)
 
 
-def test_qwen64k_index_and_quantize_bit_exact(qwen64k, head64k):
+@pytest.fixture(scope="module")
+def head64k(qwen64k, canon64k):
+    """The packed head the benchmark times."""
+    qp = dh.nvfp4_pack_head(canon64k.q, canon64k.sf)
+    return dh.DraftHead(dh.DH_FMT_NVFP4_PACKED, qwen64k.V, qp, canon64k.idx, qwen64k.n_kept, scale=canon64k.scale)
+
+
+def test_qwen64k_index_quantize_and_pack_bit_exact(qwen64k, canon64k, head64k):
     assert (qwen64k.n_kept, qwen64k.N) == (64_026, 64_064)
     q_o, sf_o, g_o = qwen64k.nvfp4()
-    assert np.array_equal(head64k.q.cpu().numpy(), q_o)
-    assert np.array_equal(head64k.sf.cpu().numpy(), sf_o)
-    assert head64k.scale.cpu().numpy()[0] == g_o
+    assert np.array_equal(canon64k.q.cpu().numpy(), q_o)
+    assert np.array_equal(canon64k.sf.cpu().numpy(), sf_o)
+    assert canon64k.scale.cpu().numpy()[0] == g_o
+    assert np.array_equal(head64k.q.cpu().numpy(), pack_reference(q_o, sf_o))
     idx_abi, nk = dh.draft_head_build_index(qwen64k.keep)
     assert nk == qwen64k.n_kept and np.array_equal(idx_abi, qwen64k.idx)
 
 
-def test_qwen64k_m1_steps(qwen64k, head64k):
+def test_qwen64k_m1_steps(qwen64k, head64k, canon64k):
     q_o, sf_o, g_o = qwen64k.nvfp4()
     for step in range(6):
         h = syn.hidden_bf16(syn.hidden_seed(1, step), 1, qwen64k.K)
         run_step(head64k, h, oracle.FMT_NVFP4, q_o, sf_o, g_o, qwen64k.idx, qwen64k.n_kept, qwen64k.V,
                  f"qwen64k M=1 step {step}")
+        if step < 2:
+            run_step(canon64k, h, oracle.FMT_NVFP4, q_o, sf_o, g_o, qwen64k.idx, qwen64k.n_kept, qwen64k.V,
+                     f"qwen64k canonical M=1 step {step}")
 
 
 @pytest.mark.parametrize("M", [1, 2, 4, 8, 16])

@@ -37,10 +37,23 @@ def tiny():
     return Workload(syn.SEED_HEAD_TINY, c["V"], c["K"], c["n_kept"], c["forced"], syn.SEED_KEEP_TINY)
 
 
-def gpu_nvfp4(wl):
+def pack_reference(q, sf):
+    """Tile-major layout written out with numpy: per (16-row tile, 128-k window),
+    the 16 rows' 64 code bytes, then their 8 scale bytes."""
+    N, Kh = q.shape
+    nwin = 2 * Kh // 128
+    codes = q.reshape(N // 16, 16, nwin, 64).transpose(0, 2, 1, 3).reshape(N // 16, nwin, 1024)
+    scales = sf.reshape(N // 16, 16, nwin, 8).transpose(0, 2, 1, 3).reshape(N // 16, nwin, 128)
+    return np.concatenate([codes, scales], axis=2)
+
+
+def gpu_nvfp4(wl, packed=False):
     W = dev_bf16(wl.W)
     idx = dev(wl.idx)
     q, sf, g = dh.nvfp4_quantize_rows(W, idx)
+    if packed:
+        qp = dh.nvfp4_pack_head(q, sf)
+        return dh.DraftHead(dh.DH_FMT_NVFP4_PACKED, wl.V, qp, idx, wl.n_kept, scale=g), (q, sf, g)
     return dh.DraftHead(dh.DH_FMT_NVFP4, wl.V, q, idx, wl.n_kept, sf=sf, scale=g), (q, sf, g)
 
 
@@ -91,14 +104,21 @@ def test_tiny_fp8_quantize_bit_exact(tiny):
     assert s.cpu().numpy()[0] == s_o
 
 
+def test_tiny_pack_bit_exact(tiny):
+    head, (q, sf, g) = gpu_nvfp4(tiny, packed=True)
+    q_o, sf_o, _ = tiny.nvfp4()
+    assert np.array_equal(head.q.cpu().numpy(), pack_reference(q_o, sf_o))
+
+
+@pytest.mark.parametrize("packed", [False, True])
 @pytest.mark.parametrize("M", [1, 2, 3, 4, 8, 13, 16])
-def test_tiny_nvfp4_step(tiny, M):
-    head, _ = gpu_nvfp4(tiny)
+def test_tiny_nvfp4_step(tiny, M, packed):
+    head, _ = gpu_nvfp4(tiny, packed)
     q_o, sf_o, g_o = tiny.nvfp4()
     for step in range(3):
         h = syn.hidden_bf16(syn.hidden_seed(0, 100 * M + step), M, tiny.K)
         run_step(head, h, oracle.FMT_NVFP4, q_o, sf_o, g_o, tiny.idx, tiny.n_kept, tiny.V,
-                 f"tiny nvfp4 M={M} step={step}")
+                 f"tiny nvfp4 packed={packed} M={M} step={step}")
 
 
 @pytest.mark.parametrize("M", [1, 4, 16])
@@ -130,9 +150,13 @@ def test_edge_shapes(V, K, n_kept, forced):
     q_o, sf_o, g_o = wl.nvfp4()
     assert np.array_equal(q.cpu().numpy(), q_o) and np.array_equal(sf.cpu().numpy(), sf_o)
     assert g.cpu().numpy()[0] == g_o
+    headp, _ = gpu_nvfp4(wl, packed=True)
+    assert np.array_equal(headp.q.cpu().numpy(), pack_reference(q_o, sf_o))
     for M in (1, 5):
         h = syn.hidden_bf16(900 + M + K, M, K)
         run_step(head, h, oracle.FMT_NVFP4, q_o, sf_o, g_o, wl.idx, wl.n_kept, V, f"edge V={V} K={K} M={M}")
+        run_step(headp, h, oracle.FMT_NVFP4, q_o, sf_o, g_o, wl.idx, wl.n_kept, V,
+                 f"edge packed V={V} K={K} M={M}")
     head8, (q8, s8) = gpu_fp8(wl)
     q8_o, s8_o = wl.fp8()
     assert np.array_equal(q8.cpu().numpy(), q8_o) and s8.cpu().numpy()[0] == s8_o
@@ -141,7 +165,7 @@ def test_edge_shapes(V, K, n_kept, forced):
 
 
 def test_special_hidden_states(tiny):
-    head, _ = gpu_nvfp4(tiny)
+    head, _ = gpu_nvfp4(tiny, packed=True)
     q_o, sf_o, g_o = tiny.nvfp4()
     K = tiny.K
     h = np.zeros((4, K), np.uint16)
@@ -166,7 +190,7 @@ def test_same_hidden_rows_agree(tiny):
 
 
 def test_cuda_graph_replay(tiny):
-    head, _ = gpu_nvfp4(tiny)
+    head, _ = gpu_nvfp4(tiny, packed=True)
     q_o, sf_o, g_o = tiny.nvfp4()
     M = 2
     h_static = torch.empty((M, tiny.K), dtype=torch.bfloat16, device="cuda")
