@@ -52,7 +52,7 @@ TRAFFIC = {"kernel_sha": None, "bytes_per_launch": None}
 
 def kernel_sha() -> str:
     h = hashlib.sha256()
-    for f in ("dh_gemv_mma.cuh", "dh_gemv_impl.cuh", "dh_common.cuh", "dh_gemv_nvfp4p.cu"):
+    for f in ("dh_gemv_mma.cuh", "dh_epilogue.cuh", "dh_common.cuh", "dh_gemv_nvfp4p.cu"):
         with open(os.path.join(ROOT, "nvfp4_draft_head_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]

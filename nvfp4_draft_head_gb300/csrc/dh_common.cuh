@@ -186,24 +186,3 @@ __device__ __forceinline__ void named_bar_sync(int id, int threads) {
 }
 
 }  // namespace dh
-
-// ------------------------------------------------------------------------
-// 2-D tiled TMA load (cp.async.bulk.tensor) into this CTA's shared memory.
-// The tensor map lives in kernel parameter space (__grid_constant__).
-// ------------------------------------------------------------------------
-namespace dh {
-
-__device__ __forceinline__ void tma_load_2d(void* dst, const void* tmap, int x, int y, uint64_t* bar,
-                                            uint64_t policy) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
-        " [%0], [%1, {%2, %3}], [%4], %5;"
-        :: "r"(smem_u32(dst)), "l"(tmap), "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(policy)
-        : "memory");
-}
-
-__device__ __forceinline__ void tma_prefetch_desc(const void* tmap) {
-    asm volatile("prefetch.tensormap [%0];" :: "l"(tmap) : "memory");
-}
-
-}  // namespace dh

@@ -1,5 +1,5 @@
 // Draft-step dispatch: format and hidden size -> kernel instantiation (one
-// translation unit per head format, see dh_gemv_impl.cuh), plus the -inf fill
+// translation unit per head format, see dh_gemv_mma.cuh), plus the -inf fill
 // of compute_logits.
 #include "dh_common.cuh"
 #include "dh_internal.h"

@@ -1,4 +1,4 @@
-// Draft-step kernels for the BF16 head (instantiations of dh_gemv_impl.cuh).
+// Draft-step kernels for the BF16 head (instantiations of dh_gemv_mma.cuh).
 #include "dh_gemv_mma.cuh"
 
 namespace dh {

@@ -38,7 +38,7 @@
 #include <cuda_fp16.h>
 
 #include "dh_common.cuh"
-#include "dh_gemv_impl.cuh"
+#include "dh_epilogue.cuh"
 #include "dh_internal.h"
 
 namespace dh {
@@ -63,11 +63,15 @@ struct Cfg {
     static constexpr int SFB = NV ? K / 16 : 0;               // scale bytes per head row
     static constexpr int WBLK = 16 * WB + 16 * 8;             // packed: bytes of one (tile, window) block
     static constexpr int TILE_REGS = WPW * (8 * CPR + (NV ? 4 : 0));
-    static constexpr int P = cmax(1, cmin(3, 48 / TILE_REGS));  // tiles of loads in flight
+    // register loads in flight (tiles ahead) when the code bytes come straight to registers
+    static constexpr int P = cmax(1, cmin(3, 48 / TILE_REGS));
+    // Canonical NVFP4 layout: a loader warp streams each tile's scale bytes
+    // into a shared-memory ring with 1-D bulk copies.
     static constexpr bool SCALES = (FMT == 1);
-    static constexpr int THREADS = (NW + 1 + (SCALES ? 1 : 0)) * 32;  // + reducer (+ scale loader)
-    static constexpr int SS = 6;                                       // scale-tile ring slots
-    static constexpr int SCALE_TILE = 16 * SFB;                        // scale bytes of one tile
+    static constexpr bool LOADER = SCALES;
+    static constexpr int THREADS = (NW + 1 + (LOADER ? 1 : 0)) * 32;  // + reducer (+ loader)
+    static constexpr int SLOT = 16 * SFB;                              // bytes of one ring slot
+    static constexpr int SS = 6;
     static constexpr int RS = (4 * NW * 16 * MT * 4 <= 40 * 1024) ? 4 : 2;  // partial-sum slots
     static_assert(NWIN % NW == 0, "windows must split evenly over warps");
     static_assert(K % 128 == 0, "K must be a multiple of 128");
@@ -160,16 +164,14 @@ template <int FMT, int K, int MT, bool LOGITS>
 __global__ void __launch_bounds__(Cfg<FMT, K, MT>::THREADS, 1) gemv_mma_kernel(const GemvArgs a) {
     using C = Cfg<FMT, K, MT>;
     constexpr int NW = C::NW, WPW = C::WPW, NT = C::NT, P = C::P, KW = K / 2, RS = C::RS;
-    constexpr int NTH = C::THREADS;
     constexpr int NRED = 16 * MT;  // (row, draft) results of a tile
     __shared__ float s_part[RS][NW][16][MT];
     __shared__ __align__(8) uint64_t full_p[RS];
     __shared__ __align__(8) uint64_t empty_p[RS];
     __shared__ __align__(8) uint64_t full_s[C::SS];
     __shared__ __align__(8) uint64_t empty_s[C::SS];
-    extern __shared__ __align__(16) uint8_t s_scales[];  // [SS][16 rows][K/16] (NVFP4)
+    extern __shared__ __align__(16) uint8_t s_scales[];  // [SS][16 rows][K/16] (canonical NVFP4)
     __shared__ unsigned long long s_best[NRED];
-    __shared__ float s_mul[MT];
     __shared__ unsigned long long s_cta[MT];
     __shared__ int s_abort;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -200,37 +202,41 @@ __global__ void __launch_bounds__(Cfg<FMT, K, MT>::THREADS, 1) gemv_mma_kernel(c
         s_abort = 0;
         mbar_init_fence();
     }
-    if (tid < MT) s_mul[tid] = (FMT == 3) ? 1.0f : 0.0f;
+    __syncthreads();  // barriers initialised
+    // The loader's copies of ring slot i % SS (tile i of this CTA).
+    const uint64_t pol = policy_evict_first();
+    auto issue = [&](int i) {
+        const int slot = i % C::SS;
+        const size_t tile = static_cast<size_t>(blockIdx.x) + static_cast<size_t>(i) * gridDim.x;
+        mbar_arrive_expect_tx(&full_s[slot], C::SLOT);
+        bulk_g2s(s_scales + slot * C::SLOT, a.sf + tile * C::SLOT, C::SLOT, &full_s[slot], pol);
+    };
+    int issued = 0;
+    if (C::LOADER && warp == NW + 1 && lane == 0) {
+        for (; issued < C::SS && issued < my_tiles; ++issued) issue(issued);
+    }
     // Programmatic dependent launch: everything above only touched the head,
     // which the preceding kernel in the stream does not write; h, the
     // workspace and the outputs are used only after its completion.
     asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;");
-    if (tid < MT && FMT != 3) s_mul[tid] = __ldg(a.scale);
-    __syncthreads();
     const uint32_t* h32 = reinterpret_cast<const uint32_t*>(a.h);
 
     if (warp == NW + 1) {
         // -------------------------------------------------- scale loader ----
-        // The 16 x K/16 scale bytes of a tile are contiguous: one 1-D bulk copy
-        // per tile into a ring of SS slots (their per-row 8-byte pieces would
-        // otherwise cost one L2 request per row and window).
-        if constexpr (C::SCALES) {
+        // The 16 x K/16 scale bytes of a tile are contiguous (their per-row
+        // 8-byte pieces would otherwise cost one L2 request per row and window).
+        if constexpr (C::LOADER) {
             if (lane == 0) {
-                const uint64_t pol = policy_evict_first();
-                int issued = 0;
-                for (int i = 0; i < my_tiles; ++i) {
+                for (int i = issued; i < my_tiles; ++i) {
                     const int slot = i % C::SS;
-                    if (i >= C::SS && !mbar_wait(&empty_s[slot], ((i / C::SS) - 1) & 1)) {
+                    if (!mbar_wait(&empty_s[slot], ((i / C::SS) - 1) & 1)) {
                         atomicOr(&a.ws->error, kDevErrTimeout);
                         *abort_flag = 1;
                     }
                     if (*abort_flag) break;
-                    const int tile = static_cast<int>(blockIdx.x) + i * static_cast<int>(gridDim.x);
-                    mbar_arrive_expect_tx(&full_s[slot], C::SCALE_TILE);
-                    bulk_g2s(s_scales + slot * C::SCALE_TILE, a.sf + static_cast<size_t>(tile) * C::SCALE_TILE,
-                             C::SCALE_TILE, &full_s[slot], pol);
-                    ++issued;
+                    issue(i);
+                    issued = i + 1;
                 }
                 if (*abort_flag) {  // let the copies already issued land before the CTA exits
                     for (int i = issued > C::SS ? issued - C::SS : 0; i < issued; ++i)
@@ -245,6 +251,7 @@ __global__ void __launch_bounds__(Cfg<FMT, K, MT>::THREADS, 1) gemv_mma_kernel(c
         // best key per (row, draft), or writes the logits; never blocks the
         // compute warps except when it falls RS tiles behind.
         for (int r = lane; r < NRED; r += 32) s_best[r] = 0ull;
+        const float gmul = (FMT == 3) ? 1.0f : __ldg(a.scale);
         for (int i = 0; i < my_tiles; ++i) {
             const int slot = i % RS;
             if (!*abort_flag && !mbar_wait(&full_p[slot], (i / RS) & 1)) {
@@ -252,6 +259,9 @@ __global__ void __launch_bounds__(Cfg<FMT, K, MT>::THREADS, 1) gemv_mma_kernel(c
                 *abort_flag = 1;
             }
             const int tile = static_cast<int>(blockIdx.x) + i * static_cast<int>(gridDim.x);
+            // keep dh_idx of these rows in L2 for the last CTA's id lookup
+            if (!LOGITS && lane == 0 && a.idx != nullptr)
+                asm volatile("prefetch.global.L2 [%0];" :: "l"(a.idx + tile * 16));
             for (int r = lane; r < NRED; r += 32) {
                 const int row_t = r / MT, m = r % MT;
                 float v = 0.0f;
@@ -259,7 +269,7 @@ __global__ void __launch_bounds__(Cfg<FMT, K, MT>::THREADS, 1) gemv_mma_kernel(c
                 for (int w = 0; w < NW; ++w) v += s_part[slot][w][row_t][m];
                 const int row = tile * 16 + row_t;
                 if (m < a.M && row < a.n_kept) {
-                    const float y = v * s_mul[m];
+                    const float y = v * gmul;
                     if constexpr (LOGITS) {
                         scatter_one(a, m, row, y);
                     } else {
@@ -353,7 +363,7 @@ __global__ void __launch_bounds__(Cfg<FMT, K, MT>::THREADS, 1) gemv_mma_kernel(c
                         atomicOr(&a.ws->error, kDevErrTimeout);
                         *abort_flag = 1;
                     }
-                    const uint8_t* st = s_scales + ss * C::SCALE_TILE;
+                    const uint8_t* st = s_scales + ss * C::SLOT;
 #pragma unroll
                     for (int ww = 0; ww < WPW; ++ww) {
                         const int w = warp + ww * NW;
@@ -527,7 +537,7 @@ inline cudaError_t launch_mma(const GemvArgs& a, cudaStream_t s) {
     auto kern = gemv_mma_kernel<FMT, K, MT, LOGITS>;
     const int sms = sm_count();
     if (sms <= 0) return cudaErrorInvalidDevice;
-    const size_t smem = C::SCALES ? static_cast<size_t>(C::SS) * C::SCALE_TILE : 0;
+    const size_t smem = C::LOADER ? static_cast<size_t>(C::SS) * C::SLOT : 0;
     static int occ[64] = {0};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);

@@ -52,9 +52,5 @@ cudaError_t launch_fp8_quantize(const uint16_t* W, int V, int K, const int32_t* 
 // Number of SMs of the current device (cached per device).
 int sm_count();
 
-// Encode a 2-D TMA tensor map (128 bytes at map128, 64-byte aligned) over a
-// row-major byte matrix [rows][row_bytes], boxes of box_rows x box_bytes.
-cudaError_t make_byte_tmap(void* map128, const void* base, uint64_t row_bytes, uint64_t rows,
-                           uint32_t box_bytes, uint32_t box_rows);
 
 }  // namespace dh
