@@ -45,9 +45,11 @@ FALLBACK_HBM_GBS = 6800.0
 N_ROWS, K_HID = 64_064, 2_560
 STEP_BYTES = N_ROWS * (K_HID // 2) + N_ROWS * (K_HID // 16) + 4 + 2 * K_HID + 4
 
-# DRAM traffic of one launch of the GEMV kernel from an ncu capture, valid
-# while the kernel source hashes to KERNEL_SHA (else reported as null).
-TRAFFIC = {"kernel_sha": None, "bytes_per_launch": None}
+# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum, mean of two
+# launches) of one launch of the M = 1 GEMV from the ncu capture summarised in
+# profiles/gemv_nvfp4_packed_m1_qwen64k.md; reported only while the kernel
+# sources still hash to kernel_sha (else null).
+TRAFFIC = {"kernel_sha": "0f4aa5a60a83bb34", "bytes_per_launch": 94_790_016}
 
 
 def kernel_sha() -> str:
