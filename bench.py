@@ -360,6 +360,122 @@ def run_ours(args, world, rank, local):
     del lib_loaded
 
 
+def run_suite(args):
+    """Secondary measurements (one JSON line each) of the other workloads:
+    the FP8 98,304-row head, the batch sweep, the BF16 full-vocabulary head,
+    the head build, and the tiny head. Same timing method as the main line
+    (one CUDA graph of `steps` calls, inputs rotated over copies > 4 x L2)."""
+    import torch
+
+    import nvfp4_draft_head_gb300 as dh
+    from nvfp4_draft_head_gb300 import build
+    build.build()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    steps = max(50, min(args.steps, 500))
+
+    def graph_us(calls):
+        s = torch.cuda.Stream(device=dev)
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            for c in calls[:3]:
+                c()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=s):
+                for c in calls:
+                    c()
+            g.replay()
+            s.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(s)
+            g.replay()
+            e1.record(s)
+            s.synchronize()
+        return e0.elapsed_time(e1) * 1e3 / len(calls)
+
+    def line(name, us, nbytes, extra=None):
+        d = {"suite": name, "us_per_call": us, "gbs": nbytes / (us * 1e-6) / 1e9, "bytes_per_call": nbytes}
+        if extra:
+            d.update(extra)
+        emit(d)
+
+    W, keep = workload_host()
+    Wd = torch.from_numpy(W.view(np.int16)).to(dev).view(torch.bfloat16)
+    hs = torch.from_numpy(hidden_steps(64).view(np.int16)).to(dev).view(torch.bfloat16)
+    hsM = torch.from_numpy(np.concatenate([syn.hidden_bf16(7000 + i, 16, K_HID) for i in range(8)]).view(np.int16)
+                           ).to(dev).view(torch.bfloat16).reshape(8, 16, K_HID)
+
+    # head build (quantise + pack), timed as single calls after a warm-up
+    idx_np, nk = dh.draft_head_build_index(keep)
+    idx = torch.from_numpy(idx_np).to(dev)
+    q = torch.empty((N_ROWS, K_HID // 2), dtype=torch.uint8, device=dev)
+    sf = torch.empty((N_ROWS, K_HID // 16), dtype=torch.uint8, device=dev)
+    gsc = torch.empty(1, dtype=torch.float32, device=dev)
+    packed = torch.empty((N_ROWS // 16, K_HID // 128, 1152), dtype=torch.uint8, device=dev)
+    nb = dh.lib().draft_head_quantize_workspace_bytes()
+    ws = dh._workspace(nb, dev)
+    st = torch.cuda.current_stream().cuda_stream
+
+    def quant():
+        dh.lib().nvfp4_quantize_rows(Wd.data_ptr(), Wd.shape[0], K_HID, idx.data_ptr(), N_ROWS, q.data_ptr(),
+                                     sf.data_ptr(), gsc.data_ptr(), ws.data_ptr(), nb,
+                                     torch.cuda.current_stream().cuda_stream)
+
+    def pack():
+        dh.lib().nvfp4_pack_head(q.data_ptr(), sf.data_ptr(), N_ROWS, K_HID, packed.data_ptr(),
+                                 torch.cuda.current_stream().cuda_stream)
+    del st
+    for _ in range(3):
+        quant()
+        pack()
+    torch.cuda.synchronize()
+    qbytes = 2 * (N_ROWS * K_HID * 2 + N_ROWS * 4) + N_ROWS * (K_HID // 2 + K_HID // 16) + 4
+    line("nvfp4 gather+quantise 64,064 x 2560", graph_us([quant] * 20), qbytes)
+    line("nvfp4 repack 64,064 x 2560", graph_us([pack] * 20), 2 * N_ROWS * (K_HID // 2 + K_HID // 16))
+
+    # batch sweep on the packed head (six rotating copies)
+    head = dh.nvfp4_head(Wd, keep)
+    heads = [head] + [head.with_storage(head.q.clone()) for _ in range(COPIES - 1)]
+    hb = N_ROWS * (K_HID // 2 + K_HID // 16) + 4
+    for M in (1, 2, 4, 8, 16):
+        ids = torch.empty(M, dtype=torch.int32, device=dev)
+        out = torch.empty((M, 248_320), dtype=torch.float32, device=dev)
+        calls = [(lambda i=i: heads[i % COPIES].top_tokens(hsM[i % 8, :M], ids=ids)) for i in range(steps)]
+        line(f"nvfp4 top_tokens M={M}", graph_us(calls), hb + M * (2 * K_HID + 4), {"M": M})
+        calls = [(lambda i=i: heads[i % COPIES].compute_logits(hsM[i % 8, :M], out=out)) for i in range(steps)]
+        line(f"nvfp4 compute_logits M={M}", graph_us(calls), hb + M * (2 * K_HID + 4 * 248_320), {"M": M})
+    del heads, head
+
+    # FP8 98,304-row head (three rotating copies = 755 MB)
+    c = syn.FP8_98K
+    keep8 = syn.keep_mask(syn.SEED_KEEP_98K, c["V"], c["n_kept"], c["forced"])
+    h8 = dh.fp8_head(Wd, keep8)
+    h8s = [h8] + [h8.with_storage(h8.q.clone()) for _ in range(2)]
+    fb = h8.N * K_HID + 4
+    for M in (1, 4):
+        ids = torch.empty(M, dtype=torch.int32, device=dev)
+        out = torch.empty((M, 248_320), dtype=torch.float32, device=dev)
+        calls = [(lambda i=i: h8s[i % 3].top_tokens(hsM[i % 8, :M], ids=ids)) for i in range(steps)]
+        line(f"fp8 98,304 top_tokens M={M}", graph_us(calls), fb + M * (2 * K_HID + 4), {"M": M})
+        calls = [(lambda i=i: h8s[i % 3].compute_logits(hsM[i % 8, :M], out=out)) for i in range(steps)]
+        line(f"fp8 98,304 compute_logits M={M}", graph_us(calls), fb + M * (2 * K_HID + 4 * 248_320), {"M": M})
+    del h8s, h8
+
+    # BF16 full-vocabulary head, the stock drafter read (1.27 GB > L2)
+    hf = dh.bf16_full_head(Wd)
+    ids = torch.empty(1, dtype=torch.int32, device=dev)
+    calls = [(lambda i=i: hf.top_tokens(hs[i % 64: i % 64 + 1], ids=ids)) for i in range(min(steps, 200))]
+    line("bf16 248,320 x 2560 top_tokens M=1", graph_us(calls), 248_320 * K_HID * 2 + 2 * K_HID + 4)
+
+    # tiny head (L2-resident, latency-bound)
+    ct = syn.TINY
+    Wt = torch.from_numpy(syn.head_bf16(syn.SEED_HEAD_TINY, ct["V"], ct["K"]).view(np.int16)).to(dev).view(torch.bfloat16)
+    ht = dh.nvfp4_head(Wt, syn.keep_mask(syn.SEED_KEEP_TINY, ct["V"], ct["n_kept"], ct["forced"]))
+    htid = torch.from_numpy(syn.hidden_bf16(1, 64, ct["K"]).view(np.int16)).to(dev).view(torch.bfloat16)
+    calls = [(lambda i=i: ht.top_tokens(htid[i % 64: i % 64 + 1], ids=ids)) for i in range(steps)]
+    line("tiny nvfp4 4,032 x 256 top_tokens M=1", graph_us(calls), ht.N * (ct["K"] // 2 + ct["K"] // 16))
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -368,10 +484,15 @@ def main():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--profile", action="store_true",
                     help="eager steps only, for ncu (prints no measurement)")
+    ap.add_argument("--suite", action="store_true",
+                    help="one line per secondary workload (FP8 head, batch sweep, BF16 head, head build, tiny)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     world, rank, local = dist_setup()
+    if args.suite:
+        run_suite(args)
+        return
     if args.impl == "reference":
         run_reference(args, world, rank)
     else:

@@ -89,6 +89,7 @@ typedef enum { DH_FMT_NVFP4 = 1, DH_FMT_FP8 = 2, DH_FMT_BF16 = 3, DH_FMT_NVFP4_P
  *           padding copies of row 0 and take no part in argmax or scatter.
  *   idx     dh_idx [N] int32, target id of each row. May be NULL only for a
  *           BF16 full-vocabulary head (then the row is the id, N == n_kept <= V).
+ *   flags   DH_HEAD_IDX_ASCENDING if idx[0..n_kept) is strictly ascending.
  * q and sf must be 16-byte aligned. */
 typedef struct dh_head {
     int fmt;
@@ -100,7 +101,16 @@ typedef struct dh_head {
     const uint8_t *sf;
     const float *scale;
     const int32_t *idx;
+    unsigned int flags;  /* DH_HEAD_* bits */
 } dh_head_t;
+
+/* dh_idx[0..n_kept) is strictly ascending (draft_head_build_index builds it
+ * so; keep.nonzero() yields ids in order). Lets get_top_tokens carry target ids
+ * in its argmax keys (equal logits still resolve to the lowest row, which then
+ * is the lowest id), so the final row -> id lookup drops out. Without it the
+ * results are the same. A head without idx (BF16 full vocabulary) counts as
+ * ascending. */
+#define DH_HEAD_IDX_ASCENDING 1u
 
 /* Build dh_idx on the host ("q38_draft.py", load_draft_model: keep.nonzero(),
  * pad = (-n) % 64 copies of the first kept id). keep_host: V bytes, non-zero =

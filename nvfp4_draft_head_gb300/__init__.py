@@ -26,6 +26,7 @@ DH_FMT_NVFP4, DH_FMT_FP8, DH_FMT_BF16, DH_FMT_NVFP4_PACKED = 1, 2, 3, 4
 DH_MAX_M = 16
 DH_WORKSPACE_ALIGN = 256
 DH_DEVERR_IDX = 1
+DH_HEAD_IDX_ASCENDING = 1
 
 EXPORTS = (
     "draft_head_build_index", "draft_head_quantize_workspace_bytes", "nvfp4_quantize_rows",
@@ -48,7 +49,7 @@ class DraftHeadError(RuntimeError):
 class dh_head_t(C.Structure):
     _fields_ = [("fmt", C.c_int), ("V", C.c_int), ("K", C.c_int), ("N", C.c_int),
                 ("n_kept", C.c_int), ("q", C.c_void_p), ("sf", C.c_void_p),
-                ("scale", C.c_void_p), ("idx", C.c_void_p)]
+                ("scale", C.c_void_p), ("idx", C.c_void_p), ("flags", C.c_uint)]
 
 
 def library_path() -> str:
@@ -192,8 +193,10 @@ class DraftHead:
     """
 
     def __init__(self, fmt: int, V: int, q: torch.Tensor, idx: torch.Tensor | None, n_kept: int,
-                 sf: torch.Tensor | None = None, scale: torch.Tensor | None = None):
+                 sf: torch.Tensor | None = None, scale: torch.Tensor | None = None,
+                 idx_ascending: bool = False):
         self.fmt, self.V, self.n_kept = fmt, int(V), int(n_kept)
+        self.flags = DH_HEAD_IDX_ASCENDING if idx_ascending else 0
         self.q, self.sf, self.scale, self.idx = q, sf, scale, idx
         self.N = q.shape[0]
         if fmt == DH_FMT_NVFP4_PACKED:        # [N/16, K/128, 1152]
@@ -206,7 +209,7 @@ class DraftHead:
         else:
             self.K = q.shape[1] if q.dtype == torch.bfloat16 else q.shape[1] // 2
         self.desc = dh_head_t(fmt, self.V, self.K, self.N, self.n_kept, _ptr(q), _ptr(sf),
-                              _ptr(scale), _ptr(idx))
+                              _ptr(scale), _ptr(idx), self.flags)
         self.ws_bytes = lib().draft_head_workspace_bytes(C.byref(self.desc), DH_MAX_M)
         self.ws = _workspace(self.ws_bytes, q.device)
         _check("draft_head_workspace_init",
@@ -218,7 +221,7 @@ class DraftHead:
         other.__dict__.update(self.__dict__)
         other.q, other.sf = q, (sf if sf is not None else self.sf)
         other.desc = dh_head_t(self.fmt, self.V, self.K, self.N, self.n_kept, _ptr(other.q),
-                               _ptr(other.sf), _ptr(self.scale), _ptr(self.idx))
+                               _ptr(other.sf), _ptr(self.scale), _ptr(self.idx), self.flags)
         return other
 
     def top_tokens(self, h: torch.Tensor, ids: torch.Tensor | None = None,
@@ -261,8 +264,8 @@ def nvfp4_head(W: torch.Tensor, keep, packed: bool = True, stream=None) -> Draft
     q, sf, g = nvfp4_quantize_rows(W, idx, stream)
     if packed and (W.shape[1] % 128 == 0):
         qp = nvfp4_pack_head(q, sf, stream)
-        return DraftHead(DH_FMT_NVFP4_PACKED, W.shape[0], qp, idx, nk, scale=g)
-    return DraftHead(DH_FMT_NVFP4, W.shape[0], q, idx, nk, sf=sf, scale=g)
+        return DraftHead(DH_FMT_NVFP4_PACKED, W.shape[0], qp, idx, nk, scale=g, idx_ascending=True)
+    return DraftHead(DH_FMT_NVFP4, W.shape[0], q, idx, nk, sf=sf, scale=g, idx_ascending=True)
 
 
 def fp8_head(W: torch.Tensor, keep, stream=None) -> DraftHead:
@@ -270,7 +273,7 @@ def fp8_head(W: torch.Tensor, keep, stream=None) -> DraftHead:
     idx_np, nk = draft_head_build_index(keep)
     idx = torch.from_numpy(idx_np).to(W.device)
     q, s = fp8_quantize_rows(W, idx, stream)
-    return DraftHead(DH_FMT_FP8, W.shape[0], q, idx, nk, scale=s)
+    return DraftHead(DH_FMT_FP8, W.shape[0], q, idx, nk, scale=s, idx_ascending=True)
 
 
 def bf16_full_head(W: torch.Tensor) -> DraftHead:

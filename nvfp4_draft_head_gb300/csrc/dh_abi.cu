@@ -68,6 +68,7 @@ dh::GemvArgs make_args(const dh_head_t* hd, const void* h, int M, void* ws) {
     a.sf = hd->sf;
     a.scale = hd->scale;
     a.idx = hd->idx;
+    a.idx_ascending = (hd->idx == nullptr || (hd->flags & DH_HEAD_IDX_ASCENDING)) ? 1 : 0;
     a.h = static_cast<const uint16_t*>(h);
     a.M = M;
     a.ws = static_cast<dh::Workspace*>(ws);
@@ -180,10 +181,10 @@ int draft_head_compute_logits(const dh_head_t* hd, const void* h, int M, float* 
     if (!aligned(out, 16)) return DH_ERR_ALIGN;
     if ((st = check_ws(ws, ws_bytes, sizeof(dh::Workspace))) != DH_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    cudaError_t e = dh::launch_fill_neg_inf(out, static_cast<size_t>(M) * hd->V, s);
-    if (e != cudaSuccess) return DH_ERR_CUDA;
     dh::GemvArgs a = make_args(hd, h, M, ws);
     a.out = out;
+    cudaError_t e = dh::launch_fill_neg_inf(out, static_cast<size_t>(M) * hd->V, s);
+    if (e != cudaSuccess) return DH_ERR_CUDA;
     return cuda_status(dh::launch_gemv(a, s));
 }
 

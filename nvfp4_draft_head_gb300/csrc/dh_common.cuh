@@ -173,6 +173,16 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
                  : "memory");
 }
 
+// 16-byte asynchronous copy global -> shared (both 16-byte aligned), tracked
+// per thread: cp_async_wait_all() returns once this thread's copies landed.
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" :: "r"(smem_u32(dst)), "l"(src) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
 // L2 policy for data read once per step (the head): evict first.
 __device__ __forceinline__ uint64_t policy_evict_first() {
     uint64_t p;

@@ -8,7 +8,9 @@
 
 namespace dh {
 
-// Publish the CTA's argmax keys; the last CTA maps rows to ids and resets.
+// Publish the CTA's argmax keys; the last CTA turns the winning key into an id
+// (the key carries the id itself when dh_idx is ascending, else the row) and
+// resets the workspace.
 // The keys go out as relaxed reductions; the ticket increment has acq_rel
 // semantics at GPU scope, which orders this CTA's reductions (made visible
 // CTA-wide by the barrier before it) ahead of the increment and lets the last
@@ -32,9 +34,13 @@ __device__ __forceinline__ void finish_argmax(const GemvArgs& a, const unsigned 
         const int m = threadIdx.x;
         unsigned long long k;
         asm volatile("atom.relaxed.gpu.global.exch.b64 %0, [%1], 0;" : "=l"(k) : "l"(&a.ws->keys[m]) : "memory");
-        const uint32_t row = 0xFFFFFFFFu - static_cast<uint32_t>(k & 0xFFFFFFFFull);
+        // low word: 0xFFFFFFFF - id with ascending ids, else 0xFFFFFFFF - row
+        const uint32_t low = 0xFFFFFFFFu - static_cast<uint32_t>(k & 0xFFFFFFFFull);
         int id = -1;
-        if (k != 0ull && row < static_cast<uint32_t>(a.N)) id = a.idx ? a.idx[row] : static_cast<int>(row);
+        if (k != 0ull) {
+            if (a.idx_ascending) id = static_cast<int>(low);
+            else if (low < static_cast<uint32_t>(a.N)) id = a.idx[low];
+        }
         if (id < 0 || id >= a.V) {
             atomicOr(&a.ws->error, kDevErrIdx);
             id = -1;
@@ -43,16 +49,6 @@ __device__ __forceinline__ void finish_argmax(const GemvArgs& a, const unsigned 
         if (a.top) a.top[m] = ordered_value(static_cast<uint32_t>(k >> 32));
     }
     if (threadIdx.x == 0) a.ws->ticket = 0u;
-}
-
-// Write one logit of compute_logits at out[m, idx[row]].
-__device__ __forceinline__ void scatter_one(const GemvArgs& a, int m, int row, float v) {
-    int id = a.idx ? a.idx[row] : row;
-    if (id < 0 || id >= a.V) {
-        atomicOr(&a.ws->error, kDevErrIdx);
-        return;
-    }
-    a.out[static_cast<size_t>(m) * a.V + id] = v;
 }
 
 }  // namespace dh

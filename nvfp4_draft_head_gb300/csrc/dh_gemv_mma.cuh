@@ -47,6 +47,11 @@ namespace mma {
 constexpr int cmin(int a, int b) { return a < b ? a : b; }
 constexpr int cmax(int a, int b) { return a > b ? a : b; }
 
+// Tiles per CTA whose dh_idx entries the reducer stages in shared memory
+// (a 64,064-row head on 152 SMs gives 27, a 98,304-row head 41); further
+// tiles read dh_idx from global memory.
+constexpr int kIdCap = 48;
+
 template <int FMT, int K, int MT>
 struct Cfg {
     static constexpr int NWIN = K / 128;                     // 128-wide k-windows per row
@@ -69,7 +74,8 @@ struct Cfg {
     // into a shared-memory ring with 1-D bulk copies.
     static constexpr bool SCALES = (FMT == 1);
     static constexpr bool LOADER = SCALES;
-    static constexpr int THREADS = (NW + 1 + (LOADER ? 1 : 0)) * 32;  // + reducer (+ loader)
+    static constexpr int NRW = MT >= 8 ? 4 : (MT >= 4 ? 2 : 1);          // reducer warps
+    static constexpr int THREADS = (NW + NRW + (LOADER ? 1 : 0)) * 32;  // + reducers (+ loader)
     static constexpr int SLOT = 16 * SFB;                              // bytes of one ring slot
     static constexpr int SS = 6;
     static constexpr int RS = (4 * NW * 16 * MT * 4 <= 40 * 1024) ? 4 : 2;  // partial-sum slots
@@ -174,6 +180,9 @@ __global__ void __launch_bounds__(Cfg<FMT, K, MT>::THREADS, 1) gemv_mma_kernel(c
     __shared__ unsigned long long s_best[NRED];
     __shared__ unsigned long long s_cta[MT];
     __shared__ int s_abort;
+    // dh_idx of this CTA's first kIdCap tiles: [i][0..15] the rows' ids, [i][16]
+    // the id of the row after the tile (copied when that row exists)
+    __shared__ __align__(16) int s_ids[kIdCap * 20];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int g = lane >> 2, t = lane & 3;
     const int n_tiles = a.N / 16;
@@ -193,7 +202,7 @@ __global__ void __launch_bounds__(Cfg<FMT, K, MT>::THREADS, 1) gemv_mma_kernel(c
     if (tid == 0) {
         for (int r = 0; r < RS; ++r) {
             mbar_init(&full_p[r], NW);
-            mbar_init(&empty_p[r], 1);
+            mbar_init(&empty_p[r], C::NRW);
         }
         for (int r = 0; r < C::SS; ++r) {
             mbar_init(&full_s[r], 1);
@@ -212,8 +221,22 @@ __global__ void __launch_bounds__(Cfg<FMT, K, MT>::THREADS, 1) gemv_mma_kernel(c
         bulk_g2s(s_scales + slot * C::SLOT, a.sf + tile * C::SLOT, C::SLOT, &full_s[slot], pol);
     };
     int issued = 0;
-    if (C::LOADER && warp == NW + 1 && lane == 0) {
+    if (C::LOADER && warp == NW + C::NRW && lane == 0) {
         for (; issued < C::SS && issued < my_tiles; ++issued) issue(issued);
+    }
+    // The reducer warps start copying dh_idx for their tiles now: it belongs to
+    // the head, so the copies overlap the preceding kernel's tail instead of
+    // sitting on the reducer's path once the partials arrive.
+    const int n_pre = ((LOGITS || a.idx_ascending) && a.idx != nullptr &&
+                       (reinterpret_cast<uintptr_t>(a.idx) & 15u) == 0)
+                          ? (my_tiles < kIdCap ? my_tiles : kIdCap)
+                          : 0;
+    if (warp >= NW && warp < NW + C::NRW) {
+        for (int c = (warp - NW) * 32 + lane; c < n_pre * 5; c += 32 * C::NRW) {
+            const int i = c / 5, ch = c - 5 * i;  // 16-byte chunk ch of tile i: ids 16 tile + 4 ch ..
+            const size_t e = (static_cast<size_t>(blockIdx.x) + static_cast<size_t>(i) * gridDim.x) * 16 + 4 * ch;
+            if (e + 4 <= static_cast<size_t>(a.N)) cp_async16(&s_ids[20 * i + 4 * ch], a.idx + e);
+        }
     }
     // Programmatic dependent launch: everything above only touched the head,
     // which the preceding kernel in the stream does not write; h, the
@@ -222,7 +245,7 @@ __global__ void __launch_bounds__(Cfg<FMT, K, MT>::THREADS, 1) gemv_mma_kernel(c
     asm volatile("griddepcontrol.launch_dependents;");
     const uint32_t* h32 = reinterpret_cast<const uint32_t*>(a.h);
 
-    if (warp == NW + 1) {
+    if (warp == NW + C::NRW) {
         // -------------------------------------------------- scale loader ----
         // The 16 x K/16 scale bytes of a tile are contiguous (their per-row
         // 8-byte pieces would otherwise cost one L2 request per row and window).
@@ -245,36 +268,67 @@ __global__ void __launch_bounds__(Cfg<FMT, K, MT>::THREADS, 1) gemv_mma_kernel(c
             }
             __syncwarp();
         }
-    } else if (warp == NW) {
+    } else if (warp >= NW) {
         // ------------------------------------------------------- reducer ----
         // Sums the NW partials of each tile in a fixed order and keeps the
         // best key per (row, draft), or writes the logits; never blocks the
         // compute warps except when it falls RS tiles behind.
-        for (int r = lane; r < NRED; r += 32) s_best[r] = 0ull;
+        const int rl = (warp - NW) * 32 + lane;  // this reducer thread's first (row, draft) slot
+        cp_async_wait_all();  // this thread's dh_idx copies, then everyone's
+        if constexpr (C::NRW > 1) named_bar_sync(1, 32 * C::NRW);
+        else __syncwarp();
+        for (int r = rl; r < NRED; r += 32 * C::NRW) s_best[r] = 0ull;
         const float gmul = (FMT == 3) ? 1.0f : __ldg(a.scale);
+        constexpr int SLOTS = (NRED + 32 * C::NRW - 1) / (32 * C::NRW);  // slots per reducer thread
         for (int i = 0; i < my_tiles; ++i) {
             const int slot = i % RS;
+            const int tile = static_cast<int>(blockIdx.x) + i * static_cast<int>(gridDim.x);
+            const int r0 = tile * 16;
+            // dh_idx of this tile's rows, fetched before waiting for the partials
+            int ids_[SLOTS];
+#pragma unroll
+            for (int k = 0; k < SLOTS; ++k) {
+                const int r = rl + k * 32 * C::NRW;
+                const int row = r0 + r / MT;
+                ids_[k] = ((LOGITS || a.idx_ascending) && r < NRED && row < a.n_kept)
+                              ? (i < n_pre ? s_ids[20 * i + r / MT] : (a.idx ? __ldg(a.idx + row) : row))
+                              : row;
+            }
             if (!*abort_flag && !mbar_wait(&full_p[slot], (i / RS) & 1)) {
                 atomicOr(&a.ws->error, kDevErrTimeout);
                 *abort_flag = 1;
             }
-            const int tile = static_cast<int>(blockIdx.x) + i * static_cast<int>(gridDim.x);
-            // keep dh_idx of these rows in L2 for the last CTA's id lookup
-            if (!LOGITS && lane == 0 && a.idx != nullptr)
-                asm volatile("prefetch.global.L2 [%0];" :: "l"(a.idx + tile * 16));
-            for (int r = lane; r < NRED; r += 32) {
-                const int row_t = r / MT, m = r % MT;
-                float v = 0.0f;
+            if constexpr (LOGITS) {
+#pragma unroll
+                for (int k = 0; k < SLOTS; ++k) {
+                    const int r = rl + k * 32 * C::NRW;
+                    if (r >= NRED) break;
+                    const int row_t = r / MT, m = r % MT;
+                    float v = 0.0f;
 #pragma unroll 4
-                for (int w = 0; w < NW; ++w) v += s_part[slot][w][row_t][m];
-                const int row = tile * 16 + row_t;
-                if (m < a.M && row < a.n_kept) {
-                    const float y = v * gmul;
-                    if constexpr (LOGITS) {
-                        scatter_one(a, m, row, y);
-                    } else {
-                        const unsigned long long k = argmax_key(ordered_key(y), static_cast<uint32_t>(row));
-                        if (k > s_best[r]) s_best[r] = k;
+                    for (int w = 0; w < NW; ++w) v += s_part[slot][w][row_t][m];
+                    const int row = r0 + row_t;
+                    if (m < a.M && row < a.n_kept) {
+                        // an id outside [0, V) is reported, not written
+                        const int id = ids_[k];
+                        if (id >= 0 && id < a.V) a.out[static_cast<size_t>(m) * a.V + id] = v * gmul;
+                        else atomicOr(&a.ws->error, kDevErrIdx);
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int k = 0; k < SLOTS; ++k) {
+                    const int r = rl + k * 32 * C::NRW;
+                    if (r >= NRED) break;
+                    const int row_t = r / MT, m = r % MT;
+                    float v = 0.0f;
+#pragma unroll 4
+                    for (int w = 0; w < NW; ++w) v += s_part[slot][w][row_t][m];
+                    const int row = r0 + row_t;
+                    if (m < a.M && row < a.n_kept) {
+                        // tie-break on the lower id (ascending dh_idx) or the lower row
+                        const unsigned long long key = argmax_key(ordered_key(v * gmul), static_cast<uint32_t>(ids_[k]));
+                        if (key > s_best[r]) s_best[r] = key;
                     }
                 }
             }

@@ -19,6 +19,7 @@ struct GemvArgs {
     const uint8_t* sf;
     const float* scale;
     const int32_t* idx;
+    int idx_ascending;   // idx[0..n_kept) strictly ascending (or idx == nullptr)
     const uint16_t* h;   // BF16 [M][K]
     int M;
     int32_t* ids;        // top-tokens mode

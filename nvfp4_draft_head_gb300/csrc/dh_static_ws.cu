@@ -77,6 +77,7 @@ extern "C" int draft_head_top_tokens_static(const dh_head_t* hd, const void* h, 
     a.sf = hd->sf;
     a.scale = hd->scale;
     a.idx = hd->idx;
+    a.idx_ascending = (hd->idx == nullptr || (hd->flags & DH_HEAD_IDX_ASCENDING)) ? 1 : 0;
     a.h = static_cast<const uint16_t*>(h);
     a.M = M;
     a.ids = ids;

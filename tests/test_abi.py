@@ -75,7 +75,7 @@ def _desc(**kw):
     d = dict(fmt=dh.DH_FMT_NVFP4, V=16384, K=256, N=4032, n_kept=4000, q=0x10000, sf=0x20000,
              scale=0x30000, idx=0x40000)
     d.update(kw)
-    return dh.dh_head_t(d["fmt"], d["V"], d["K"], d["N"], d["n_kept"], d["q"], d["sf"], d["scale"], d["idx"])
+    return dh.dh_head_t(d["fmt"], d["V"], d["K"], d["N"], d["n_kept"], d["q"], d["sf"], d["scale"], d["idx"], 0)
 
 
 WS = 0x100000   # a fake, never dereferenced, 256-aligned device address

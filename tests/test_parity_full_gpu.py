@@ -55,7 +55,8 @@ def canon64k(qwen64k, W_dev):
 def head64k(qwen64k, canon64k):
     """The packed head the benchmark times."""
     qp = dh.nvfp4_pack_head(canon64k.q, canon64k.sf)
-    return dh.DraftHead(dh.DH_FMT_NVFP4_PACKED, qwen64k.V, qp, canon64k.idx, qwen64k.n_kept, scale=canon64k.scale)
+    return dh.DraftHead(dh.DH_FMT_NVFP4_PACKED, qwen64k.V, qp, canon64k.idx, qwen64k.n_kept, scale=canon64k.scale,
+                        idx_ascending=True)
 
 
 def test_qwen64k_index_quantize_and_pack_bit_exact(qwen64k, canon64k, head64k):
@@ -104,7 +105,7 @@ def test_fp8_98k_head(W_full, W_dev):
     q, s = dh.fp8_quantize_rows(W_dev, idx)
     q_o, s_o = wl.fp8()
     assert np.array_equal(q.cpu().numpy(), q_o) and s.cpu().numpy()[0] == s_o
-    head = dh.DraftHead(dh.DH_FMT_FP8, wl.V, q, idx, wl.n_kept, scale=s)
+    head = dh.DraftHead(dh.DH_FMT_FP8, wl.V, q, idx, wl.n_kept, scale=s, idx_ascending=True)
     for M in (1, 4):
         h = syn.hidden_bf16(syn.hidden_seed(2, M), M, wl.K)
         run_step(head, h, oracle.FMT_FP8, q_o, None, s_o, wl.idx, wl.n_kept, wl.V, f"fp8 98k M={M}")

@@ -47,21 +47,25 @@ def pack_reference(q, sf):
     return np.concatenate([codes, scales], axis=2)
 
 
-def gpu_nvfp4(wl, packed=False):
+def gpu_nvfp4(wl, packed=False, ascending=None):
+    """NVFP4 head on the GPU; by default the packed head declares its dh_idx
+    ascending (argmax keys carry ids, dh_idx staged in shared memory) and the
+    canonical one does not, so both code paths of the draft step run."""
     W = dev_bf16(wl.W)
     idx = dev(wl.idx)
     q, sf, g = dh.nvfp4_quantize_rows(W, idx)
+    asc = packed if ascending is None else ascending
     if packed:
         qp = dh.nvfp4_pack_head(q, sf)
-        return dh.DraftHead(dh.DH_FMT_NVFP4_PACKED, wl.V, qp, idx, wl.n_kept, scale=g), (q, sf, g)
-    return dh.DraftHead(dh.DH_FMT_NVFP4, wl.V, q, idx, wl.n_kept, sf=sf, scale=g), (q, sf, g)
+        return dh.DraftHead(dh.DH_FMT_NVFP4_PACKED, wl.V, qp, idx, wl.n_kept, scale=g, idx_ascending=asc), (q, sf, g)
+    return dh.DraftHead(dh.DH_FMT_NVFP4, wl.V, q, idx, wl.n_kept, sf=sf, scale=g, idx_ascending=asc), (q, sf, g)
 
 
-def gpu_fp8(wl):
+def gpu_fp8(wl, ascending=True):
     W = dev_bf16(wl.W)
     idx = dev(wl.idx)
     q, s = dh.fp8_quantize_rows(W, idx)
-    return dh.DraftHead(dh.DH_FMT_FP8, wl.V, q, idx, wl.n_kept, scale=s), (q, s)
+    return dh.DraftHead(dh.DH_FMT_FP8, wl.V, q, idx, wl.n_kept, scale=s, idx_ascending=ascending), (q, s)
 
 
 def run_step(head, h_bits, fmt, q_or, sf_or, s_or, idx, n_kept, V, what):
@@ -121,12 +125,14 @@ def test_tiny_nvfp4_step(tiny, M, packed):
                  f"tiny nvfp4 packed={packed} M={M} step={step}")
 
 
+@pytest.mark.parametrize("ascending", [False, True])
 @pytest.mark.parametrize("M", [1, 4, 16])
-def test_tiny_fp8_step(tiny, M):
-    head, _ = gpu_fp8(tiny)
+def test_tiny_fp8_step(tiny, M, ascending):
+    head, _ = gpu_fp8(tiny, ascending)
     q_o, s_o = tiny.fp8()
     h = syn.hidden_bf16(syn.hidden_seed(0, 500 + M), M, tiny.K)
-    run_step(head, h, oracle.FMT_FP8, q_o, None, s_o, tiny.idx, tiny.n_kept, tiny.V, f"tiny fp8 M={M}")
+    run_step(head, h, oracle.FMT_FP8, q_o, None, s_o, tiny.idx, tiny.n_kept, tiny.V,
+             f"tiny fp8 M={M} ascending={ascending}")
 
 
 @pytest.mark.parametrize("M", [1, 2, 16])
@@ -220,9 +226,13 @@ def test_out_of_range_idx_sets_the_error_word(tiny):
     bad[5] = tiny.V            # one kept row points past the vocabulary
     idx_bad = dev(bad)
     head_bad = dh.DraftHead(dh.DH_FMT_NVFP4, tiny.V, q, idx_bad, tiny.n_kept, sf=sf, scale=g)
+    head_bad_asc = dh.DraftHead(dh.DH_FMT_NVFP4, tiny.V, q, idx_bad, tiny.n_kept, sf=sf, scale=g,
+                                idx_ascending=True)
     h = dev_bf16(syn.hidden_bf16(3, 1, tiny.K))
     head_bad.compute_logits(h)
     assert head_bad.device_error() == dh.DH_DEVERR_IDX
     assert head_bad.device_error() == 0                        # reading clears it
+    head_bad_asc.compute_logits(h)                             # ids staged in shared memory too
+    assert head_bad_asc.device_error() == dh.DH_DEVERR_IDX
     with pytest.raises(RuntimeError, match="device error"):
         dh.nvfp4_quantize_rows(dev_bf16(tiny.W), idx_bad)
