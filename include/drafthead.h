@@ -37,7 +37,7 @@
  *     Read them with draft_head_read_device_error.
  *   - Ids are int32 (V < 2^31); the pages' int64 ids have the same values.
  *   - One call at a time per workspace: two calls in flight on the GPU that
- *     share a workspace race on its argmax keys.
+ *     share a workspace race on its argmax slots.
  */
 #ifndef DRAFTHEAD_H
 #define DRAFTHEAD_H
@@ -65,7 +65,8 @@ typedef enum {
 } dh_status;
 
 /* Bits of the device error word. */
-#define DH_DEVERR_IDX 1u  /* a dh_idx entry was outside [0, V) */
+#define DH_DEVERR_IDX 1u      /* a dh_idx entry was outside [0, V) */
+#define DH_DEVERR_TIMEOUT 2u  /* a bounded device wait gave up (results invalid) */
 
 typedef enum { DH_FMT_NVFP4 = 1, DH_FMT_FP8 = 2, DH_FMT_BF16 = 3, DH_FMT_NVFP4_PACKED = 4 } dh_format;
 
@@ -160,8 +161,9 @@ int nvfp4_pack_head(const uint8_t *q, const uint8_t *sf, int N, int K, uint8_t *
 /* Bytes of workspace the draft-step calls need for up to M_max drafts. */
 size_t draft_head_workspace_bytes(const dh_head_t *hd, int M_max);
 
-/* Zero a draft-step workspace (argmax keys, ticket, error word). Call once
- * after allocating it; every later call leaves it zeroed again. */
+/* Zero a draft-step workspace (error word, per-CTA argmax slots). Call once
+ * after allocating it; every later call leaves the slots zeroed again. After
+ * a DH_DEVERR_TIMEOUT, call it again before the next draft step. */
 int draft_head_workspace_init(void *ws, size_t ws_bytes, void *stream);
 
 /* get_top_tokens ("q38_draft.py"): for each draft m < M,
@@ -187,13 +189,14 @@ int draft_head_compute_logits(const dh_head_t *hd, const void *h, int M, float *
  * output buffers, or a serving loop that forbids cudaMalloc because it can
  * synchronise the device. The paper has no counterpart of this entry point.
  * Same arguments and results as draft_head_top_tokens, minus the workspace.
- * Its scratch is one fixed 256-byte array inside the library (argmax keys for
- * at most DH_MAX_M = 16 drafts, a ticket, an error word); every GPU that loads
- * the library holds it until the process exits. M > 16 returns DH_ERR_SHAPE.
+ * Its scratch is one fixed array inside the library, laid out as a
+ * draft-step workspace (argmax slots for at most DH_MAX_M = 16 drafts, an
+ * error word; draft_head_workspace_bytes() bytes); every GPU that loads the
+ * library holds it until the process exits. M > 16 returns DH_ERR_SHAPE.
  * The first call on a device looks up the array's device address
  * (cudaGetSymbolAddress) with that device current; make that first call
- * before any stream capture. Each call clears the keys and the ticket with
- * cudaMemsetAsync on `stream`, then launches the kernel; nothing is allocated.
+ * before any stream capture. Each call launches the kernel alone (the slots
+ * are zero at load and each launch zeroes them again); nothing is allocated.
  * All calls share the one array, so calls that overlap on the GPU (other
  * streams, other threads) race and give wrong ids: serialise them. An id of
  * -1 marks a winning row whose dh_idx entry was outside [0, V). */

@@ -26,6 +26,7 @@ DH_FMT_NVFP4, DH_FMT_FP8, DH_FMT_BF16, DH_FMT_NVFP4_PACKED = 1, 2, 3, 4
 DH_MAX_M = 16
 DH_WORKSPACE_ALIGN = 256
 DH_DEVERR_IDX = 1
+DH_DEVERR_TIMEOUT = 2
 DH_HEAD_IDX_ASCENDING = 1
 
 EXPORTS = (

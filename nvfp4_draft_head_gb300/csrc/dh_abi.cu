@@ -114,7 +114,7 @@ int draft_head_build_index(const uint8_t* keep_host, int V, int32_t* idx_host, i
     return DH_OK;
 }
 
-size_t draft_head_quantize_workspace_bytes(void) { return sizeof(dh::Workspace); }
+size_t draft_head_quantize_workspace_bytes(void) { return dh::kWorkspaceHeader; }
 
 int nvfp4_quantize_rows(const void* W, int V, int K, const int32_t* idx, int N, uint8_t* q,
                         uint8_t* sf, float* g, void* ws, size_t ws_bytes, void* stream) {
@@ -122,7 +122,7 @@ int nvfp4_quantize_rows(const void* W, int V, int K, const int32_t* idx, int N, 
     if (st != DH_OK) return st;
     if (q == nullptr || sf == nullptr || g == nullptr) return DH_ERR_ARG;
     if (!aligned(q, 16) || !aligned(sf, 16) || !aligned(g, 4)) return DH_ERR_ALIGN;
-    if ((st = check_ws(ws, ws_bytes, sizeof(dh::Workspace))) != DH_OK) return st;
+    if ((st = check_ws(ws, ws_bytes, dh::kWorkspaceHeader)) != DH_OK) return st;
     return cuda_status(dh::launch_nvfp4_quantize(static_cast<const uint16_t*>(W), V, K, idx, N, q, sf,
                                                  g, static_cast<dh::Workspace*>(ws),
                                                  static_cast<cudaStream_t>(stream)));
@@ -134,7 +134,7 @@ int fp8_quantize_rows(const void* W, int V, int K, const int32_t* idx, int N, ui
     if (st != DH_OK) return st;
     if (q == nullptr || scale == nullptr) return DH_ERR_ARG;
     if (!aligned(q, 16) || !aligned(scale, 4)) return DH_ERR_ALIGN;
-    if ((st = check_ws(ws, ws_bytes, sizeof(dh::Workspace))) != DH_OK) return st;
+    if ((st = check_ws(ws, ws_bytes, dh::kWorkspaceHeader)) != DH_OK) return st;
     return cuda_status(dh::launch_fp8_quantize(static_cast<const uint16_t*>(W), V, K, idx, N, q, scale,
                                                static_cast<dh::Workspace*>(ws),
                                                static_cast<cudaStream_t>(stream)));

@@ -1,21 +1,29 @@
 // Device helpers shared by the draft-head kernels (CUDA side only).
 #pragma once
 
+#include <cstddef>
 #include <cstdint>
 #include <cuda_runtime.h>
 #include <cuda_fp16.h>
 
 namespace dh {
 
-// Layout of a draft-step workspace (first 256 bytes; callers allocate it).
+// CTAs a draft-step launch may use (the launcher caps its grid here).
+constexpr int kMaxGrid = 1024;
+
+// Layout of a workspace (callers allocate it). The quantisers use only the
+// 256-byte header; a draft step also uses the slots, which start at zero and
+// which the collecting CTA zeroes again after reading them.
 struct Workspace {
-    unsigned long long keys[16];  // per draft: max over rows of (ordered logit << 32 | ~row)
-    unsigned int ticket;          // CTAs that have published their keys this launch
-    unsigned int error;           // DH_DEVERR_* bits
-    unsigned int amax_bits;       // quantisers: running max |w| as float bits
-    unsigned int pad_[29];
+    unsigned int error;      // DH_DEVERR_* bits
+    unsigned int amax_bits;  // quantisers: running max |w| as float bits
+    unsigned int pad_[62];
+    // per draft and CTA: the CTA's best (ordered logit << 32 | ~id or ~row)
+    // key, or 1 when it holds no kept row; 0 while not yet published
+    unsigned long long slots[16][kMaxGrid];
 };
-static_assert(sizeof(Workspace) == 256, "workspace header is 256 bytes");
+constexpr size_t kWorkspaceHeader = 256;
+static_assert(offsetof(Workspace, slots) == kWorkspaceHeader, "workspace header is 256 bytes");
 
 constexpr unsigned int kDevErrIdx = 1u;
 

@@ -8,32 +8,43 @@
 
 namespace dh {
 
-// Publish the CTA's argmax keys; the last CTA turns the winning key into an id
-// (the key carries the id itself when dh_idx is ascending, else the row) and
-// resets the workspace.
-// The keys go out as relaxed reductions; the ticket increment has acq_rel
-// semantics at GPU scope, which orders this CTA's reductions (made visible
-// CTA-wide by the barrier before it) ahead of the increment and lets the last
-// CTA see every other CTA's keys, without a separate fence round trip.
+// Grid-wide argmax hand-off. Every CTA stores its best key per draft in its
+// own workspace slot (1 when it holds no kept row). CTA 0 polls all slots
+// until each is non-zero, zeroes them for the next launch, keeps the maximum
+// and turns it into an id (the key carries the id itself when dh_idx is
+// ascending, else the row). The key is its own "published" flag, so the
+// hand-off costs one store and one poll round trip, with no fence, ticket or
+// read-back after it.
 __device__ __forceinline__ void finish_argmax(const GemvArgs& a, const unsigned long long* cta_key) {
-    __shared__ bool s_last;
     if (threadIdx.x < a.M) {
-        if (cta_key[threadIdx.x] != 0ull)
-            asm volatile("red.relaxed.gpu.global.max.u64 [%0], %1;"
-                         :: "l"(&a.ws->keys[threadIdx.x]), "l"(cta_key[threadIdx.x]) : "memory");
+        const unsigned long long k = cta_key[threadIdx.x] != 0ull ? cta_key[threadIdx.x] : 1ull;
+        asm volatile("st.relaxed.gpu.global.u64 [%0], %1;"
+                     :: "l"(&a.ws->slots[threadIdx.x][blockIdx.x]), "l"(k) : "memory");
+    }
+    if (blockIdx.x != 0) return;
+    __shared__ unsigned long long s_red[16];
+    __shared__ int s_late;
+    if (threadIdx.x < 16) s_red[threadIdx.x] = 0ull;
+    if (threadIdx.x == 0) s_late = 0;
+    __syncthreads();
+    const int G = static_cast<int>(gridDim.x);
+    for (int j = threadIdx.x; j < G * a.M; j += blockDim.x) {
+        const int m = j / G, b = j - m * G;
+        unsigned long long* p = &a.ws->slots[m][b];
+        unsigned long long v = 0ull;
+        for (uint32_t n = 0; n < kWaitLimit; ++n) {
+            asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+            if (v != 0ull) break;
+        }
+        if (v == 0ull) s_late = 1;
+        asm volatile("st.relaxed.gpu.global.u64 [%0], 0;" :: "l"(p) : "memory");
+        if (v > 1ull) atomicMax(&s_red[m], v);
     }
     __syncthreads();
-    if (threadIdx.x == 0) {
-        unsigned int t;
-        asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(t) : "l"(&a.ws->ticket) : "memory");
-        s_last = (t == gridDim.x - 1);
-    }
-    __syncthreads();
-    if (!s_last) return;
+    if (threadIdx.x == 0 && s_late) atomicOr(&a.ws->error, kDevErrTimeout);
     if (threadIdx.x < a.M) {
         const int m = threadIdx.x;
-        unsigned long long k;
-        asm volatile("atom.relaxed.gpu.global.exch.b64 %0, [%1], 0;" : "=l"(k) : "l"(&a.ws->keys[m]) : "memory");
+        const unsigned long long k = s_red[m];
         // low word: 0xFFFFFFFF - id with ascending ids, else 0xFFFFFFFF - row
         const uint32_t low = 0xFFFFFFFFu - static_cast<uint32_t>(k & 0xFFFFFFFFull);
         int id = -1;
@@ -48,7 +59,6 @@ __device__ __forceinline__ void finish_argmax(const GemvArgs& a, const unsigned 
         a.ids[m] = id;
         if (a.top) a.top[m] = ordered_value(static_cast<uint32_t>(k >> 32));
     }
-    if (threadIdx.x == 0) a.ws->ticket = 0u;
 }
 
 }  // namespace dh

@@ -608,6 +608,7 @@ inline cudaError_t launch_mma(const GemvArgs& a, cudaStream_t s) {
     const int n_tiles = a.N / 16;
     int blocks = sms * occ[dev];
     if (blocks > n_tiles) blocks = n_tiles;
+    if (blocks > kMaxGrid) blocks = kMaxGrid;  // one argmax slot per CTA
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(blocks);
     cfg.blockDim = dim3(C::THREADS);

@@ -1,9 +1,9 @@
 // draft_head_top_tokens_static: the get_top_tokens draft step for callers that
 // cannot allocate device memory (a plugin hook that is handed only its input
 // and output buffers, or a serving loop that forbids cudaMalloc because it can
-// synchronise the device). Its scratch (the per-draft argmax keys, the
-// last-CTA ticket and the device error word) lives in a fixed array of this
-// library instead of a caller-provided workspace.
+// synchronise the device). Its scratch (the per-draft, per-CTA argmax slots
+// and the device error word) lives in a fixed array of this library instead
+// of a caller-provided workspace.
 #include <cstddef>
 #include <cstdint>
 #include <cuda_runtime.h>
@@ -14,8 +14,9 @@
 
 namespace {
 
-// 256 bytes of scratch: argmax keys for up to DH_MAX_M drafts, the ticket and
-// the error word. Every GPU that loads the library holds it until the process
+// Scratch laid out as a draft-step workspace: the error word and argmax slots
+// for up to DH_MAX_M drafts (zero at load; each launch zeroes the slots it
+// used again). Every GPU that loads the library holds it until the process
 // exits. In host code this name is only a host-side stand-in for the array:
 // the device address comes from cudaGetSymbolAddress.
 static __device__ __align__(256) unsigned char g_static_scratch[sizeof(dh::Workspace)];
@@ -42,7 +43,7 @@ int static_scratch(void** out) {
 extern "C" int draft_head_top_tokens_static(const dh_head_t* hd, const void* h, int M, int32_t* ids,
                                             float* top_logit, void* stream) {
     if (hd == nullptr || h == nullptr || ids == nullptr) return DH_ERR_ARG;
-    if (M < 1 || M > DH_MAX_M) return DH_ERR_SHAPE;  // the scratch holds keys for 16 drafts
+    if (M < 1 || M > DH_MAX_M) return DH_ERR_SHAPE;  // the scratch holds slots for 16 drafts
     if (hd->q == nullptr) return DH_ERR_ARG;
     if (hd->fmt != DH_FMT_NVFP4 && hd->fmt != DH_FMT_FP8 && hd->fmt != DH_FMT_BF16 && hd->fmt != DH_FMT_NVFP4_PACKED)
         return DH_ERR_ARG;
@@ -63,9 +64,6 @@ extern "C" int draft_head_top_tokens_static(const dh_head_t* hd, const void* h, 
     int st = static_scratch(&scratch);
     if (st != DH_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    // The array keeps whatever the previous call left; the keys and the ticket
-    // must start at zero.
-    if (cudaMemsetAsync(scratch, 0, offsetof(dh::Workspace, error), s) != cudaSuccess) return DH_ERR_CUDA;
 
     dh::GemvArgs a{};
     a.fmt = hd->fmt;
