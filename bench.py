@@ -41,7 +41,8 @@ FALLBACK_HBM_GBS = 6800.0
 
 # Algorithmic bytes of one draft step at M = 1: NVFP4 codes (64,064 x 1,280 B)
 # + E4M3 block scales (64,064 x 160 B) + g (4 B) + h (2,560 x 2 B) + the id (4 B).
-# dh_idx is read only for the winning row.
+# The method needs dh_idx only for the winning row; the kernel stages all of it
+# (256 KB, L2-resident from step to step) so that its argmax keys carry ids.
 N_ROWS, K_HID = 64_064, 2_560
 STEP_BYTES = N_ROWS * (K_HID // 2) + N_ROWS * (K_HID // 16) + 4 + 2 * K_HID + 4
 
@@ -49,7 +50,7 @@ STEP_BYTES = N_ROWS * (K_HID // 2) + N_ROWS * (K_HID // 16) + 4 + 2 * K_HID + 4
 # launches) of one launch of the M = 1 GEMV from the ncu capture summarised in
 # profiles/gemv_nvfp4_packed_m1_qwen64k.md; reported only while the kernel
 # sources still hash to kernel_sha (else null).
-TRAFFIC = {"kernel_sha": "0f4aa5a60a83bb34", "bytes_per_launch": 94_790_016}
+TRAFFIC = {"kernel_sha": "334f9e3e2ba6e35d", "bytes_per_launch": 94_891_648}
 
 
 def kernel_sha() -> str:
