@@ -16,9 +16,10 @@
 // head rows g and g+8 of the tile, the 32 consecutive k of each of its windows
 // starting at 32 t (one 16-byte load per row for NVFP4). Loads of the next
 // P-1 tiles are in flight while a tile is computed. Per-warp partial logits go
-// to shared memory (double-buffered by tile parity); after one __syncthreads
-// per tile, 16 x MT reducer threads sum the NW partials, keep the best
-// (logit, row) key of their (row, draft), or write the logit into out[m, idx].
+// to a ring of RS shared-memory slots guarded by mbarriers; reducer warps sum
+// the NW partials of each (row, draft) in a fixed order (two drafts per
+// float2 read at 16 drafts), keep the best (logit, id or row) key of each, or
+// write the logit into out[m, idx].
 //
 // NVFP4 with one draft (the headline case) uses a block-diagonal B: the 8
 // columns of the MMA are the 8 E4M3 blocks of a window instead of 8 drafts.
@@ -68,13 +69,17 @@ struct Cfg {
     static constexpr int SFB = NV ? K / 16 : 0;               // scale bytes per head row
     static constexpr int WBLK = 16 * WB + 16 * 8;             // packed: bytes of one (tile, window) block
     static constexpr int TILE_REGS = WPW * (8 * CPR + (NV ? 4 : 0));
-    // register loads in flight (tiles ahead) when the code bytes come straight to registers
-    static constexpr int P = cmax(1, cmin(3, 48 / TILE_REGS));
+    // register loads in flight (tiles ahead) when the code bytes come straight to
+    // registers; two at 16 drafts, where the h fragments of two n8 tiles leave no
+    // room for a third within the 80 registers 21+ warps per SM allow
+    static constexpr int P = cmax(1, cmin(MT >= 16 ? 2 : 3, 48 / TILE_REGS));
     // Canonical NVFP4 layout: a loader warp streams each tile's scale bytes
     // into a shared-memory ring with 1-D bulk copies.
     static constexpr bool SCALES = (FMT == 1);
     static constexpr bool LOADER = SCALES;
-    static constexpr int NRW = MT >= 8 ? 4 : (MT >= 4 ? 2 : 1);          // reducer warps
+    // reducer unit: one row and DV drafts (one float2 read per partial at 16 drafts)
+    static constexpr int DV = MT >= 16 ? 2 : 1;
+    static constexpr int NRW = MT >= 16 ? (16 * MT / DV) / 32 : (MT >= 8 ? 4 : (MT >= 4 ? 2 : 1));  // reducer warps
     static constexpr int THREADS = (NW + NRW + (LOADER ? 1 : 0)) * 32;  // + reducers (+ loader)
     static constexpr int SLOT = 16 * SFB;                              // bytes of one ring slot
     static constexpr int SS = 6;
@@ -171,7 +176,7 @@ __global__ void __launch_bounds__(Cfg<FMT, K, MT>::THREADS, 1) gemv_mma_kernel(c
     using C = Cfg<FMT, K, MT>;
     constexpr int NW = C::NW, WPW = C::WPW, NT = C::NT, P = C::P, KW = K / 2, RS = C::RS;
     constexpr int NRED = 16 * MT;  // (row, draft) results of a tile
-    __shared__ float s_part[RS][NW][16][MT];
+    __shared__ __align__(16) float s_part[RS][NW][16][MT];
     __shared__ __align__(8) uint64_t full_p[RS];
     __shared__ __align__(8) uint64_t empty_p[RS];
     __shared__ __align__(8) uint64_t full_s[C::SS];
@@ -273,13 +278,16 @@ __global__ void __launch_bounds__(Cfg<FMT, K, MT>::THREADS, 1) gemv_mma_kernel(c
         // Sums the NW partials of each tile in a fixed order and keeps the
         // best key per (row, draft), or writes the logits; never blocks the
         // compute warps except when it falls RS tiles behind.
-        const int rl = (warp - NW) * 32 + lane;  // this reducer thread's first (row, draft) slot
+        const int rl = (warp - NW) * 32 + lane;  // this reducer thread's first unit
         cp_async_wait_all();  // this thread's dh_idx copies, then everyone's
         if constexpr (C::NRW > 1) named_bar_sync(1, 32 * C::NRW);
         else __syncwarp();
         for (int r = rl; r < NRED; r += 32 * C::NRW) s_best[r] = 0ull;
         const float gmul = (FMT == 3) ? 1.0f : __ldg(a.scale);
-        constexpr int SLOTS = (NRED + 32 * C::NRW - 1) / (32 * C::NRW);  // slots per reducer thread
+        constexpr int DV = C::DV;
+        constexpr int UPR = MT / DV;                                    // units per row
+        constexpr int NU = 16 * UPR;                                     // units per tile
+        constexpr int SLOTS = (NU + 32 * C::NRW - 1) / (32 * C::NRW);  // units per reducer thread
         for (int i = 0; i < my_tiles; ++i) {
             const int slot = i % RS;
             const int tile = static_cast<int>(blockIdx.x) + i * static_cast<int>(gridDim.x);
@@ -288,46 +296,57 @@ __global__ void __launch_bounds__(Cfg<FMT, K, MT>::THREADS, 1) gemv_mma_kernel(c
             int ids_[SLOTS];
 #pragma unroll
             for (int k = 0; k < SLOTS; ++k) {
-                const int r = rl + k * 32 * C::NRW;
-                const int row = r0 + r / MT;
-                ids_[k] = ((LOGITS || a.idx_ascending) && r < NRED && row < a.n_kept)
-                              ? (i < n_pre ? s_ids[20 * i + r / MT] : (a.idx ? __ldg(a.idx + row) : row))
+                const int u = rl + k * 32 * C::NRW;
+                const int row = r0 + u / UPR;
+                ids_[k] = ((LOGITS || a.idx_ascending) && u < NU && row < a.n_kept)
+                              ? (i < n_pre ? s_ids[20 * i + u / UPR] : (a.idx ? __ldg(a.idx + row) : row))
                               : row;
             }
             if (!*abort_flag && !mbar_wait(&full_p[slot], (i / RS) & 1)) {
                 atomicOr(&a.ws->error, kDevErrTimeout);
                 *abort_flag = 1;
             }
-            if constexpr (LOGITS) {
 #pragma unroll
-                for (int k = 0; k < SLOTS; ++k) {
-                    const int r = rl + k * 32 * C::NRW;
-                    if (r >= NRED) break;
-                    const int row_t = r / MT, m = r % MT;
-                    float v = 0.0f;
+            for (int k = 0; k < SLOTS; ++k) {
+                const int u = rl + k * 32 * C::NRW;
+                if (u >= NU) break;
+                const int row_t = u / UPR, m0 = (u % UPR) * DV;
+                // fixed summation order over the warps, the same for every draft
+                float v[DV];
+#pragma unroll
+                for (int d = 0; d < DV; ++d) v[d] = 0.0f;
 #pragma unroll 4
-                    for (int w = 0; w < NW; ++w) v += s_part[slot][w][row_t][m];
-                    const int row = r0 + row_t;
-                    if (m < a.M && row < a.n_kept) {
-                        // an id outside [0, V) is reported, not written
-                        const int id = ids_[k];
-                        if (id >= 0 && id < a.V) a.out[static_cast<size_t>(m) * a.V + id] = v * gmul;
-                        else atomicOr(&a.ws->error, kDevErrIdx);
+                for (int w = 0; w < NW; ++w) {
+                    if constexpr (DV == 4) {
+                        const float4 q4 = *reinterpret_cast<const float4*>(&s_part[slot][w][row_t][m0]);
+                        v[0] += q4.x;
+                        v[1] += q4.y;
+                        v[2] += q4.z;
+                        v[3] += q4.w;
+                    } else if constexpr (DV == 2) {
+                        const float2 q2 = *reinterpret_cast<const float2*>(&s_part[slot][w][row_t][m0]);
+                        v[0] += q2.x;
+                        v[1] += q2.y;
+                    } else {
+                        v[0] += s_part[slot][w][row_t][m0];
                     }
                 }
-            } else {
+                const int row = r0 + row_t;
+                if (row >= a.n_kept) continue;
 #pragma unroll
-                for (int k = 0; k < SLOTS; ++k) {
-                    const int r = rl + k * 32 * C::NRW;
-                    if (r >= NRED) break;
-                    const int row_t = r / MT, m = r % MT;
-                    float v = 0.0f;
-#pragma unroll 4
-                    for (int w = 0; w < NW; ++w) v += s_part[slot][w][row_t][m];
-                    const int row = r0 + row_t;
-                    if (m < a.M && row < a.n_kept) {
+                for (int d = 0; d < DV; ++d) {
+                    const int m = m0 + d;
+                    if (m >= a.M) break;
+                    if constexpr (LOGITS) {
+                        // an id outside [0, V) is reported, not written
+                        const int id = ids_[k];
+                        if (id >= 0 && id < a.V) a.out[static_cast<size_t>(m) * a.V + id] = v[d] * gmul;
+                        else atomicOr(&a.ws->error, kDevErrIdx);
+                    } else {
                         // tie-break on the lower id (ascending dh_idx) or the lower row
-                        const unsigned long long key = argmax_key(ordered_key(v * gmul), static_cast<uint32_t>(ids_[k]));
+                        const unsigned long long key =
+                            argmax_key(ordered_key(v[d] * gmul), static_cast<uint32_t>(ids_[k]));
+                        const int r = row_t * MT + m;
                         if (key > s_best[r]) s_best[r] = key;
                     }
                 }
