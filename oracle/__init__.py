@@ -61,6 +61,8 @@ def _L():
             lib.or_nvfp4_quantize.argtypes = [P, i, i, P, i, P, P, P]
             lib.or_fp8_quantize.argtypes = [P, i, i, P, i, P, P]
             lib.or_gemv.argtypes = [i, P, P, f, i, i, P, i, P, P]
+            lib.or_fp8_act_quantize.argtypes = [P, i, i, P, P]
+            lib.or_gemv_w8a8.argtypes = [P, f, i, i, P, P, i, P, P]
             lib.or_argmax.argtypes = [P, i]
             lib.or_top_tokens.argtypes = [P, i, i, P, P, P]
             lib.or_scatter_logits.argtypes = [P, i, i, P, i, i, P]
@@ -138,7 +140,34 @@ def fp8_quantize(W: np.ndarray, idx: np.ndarray):
     return q, np.float32(s.value)
 
 
+def fp8_act_quantize(h: np.ndarray):
+    """(qx uint8[M, K], sx float32[M]): per-token E4M3 codes and scales of the
+    BF16 hidden states h (uint16 bits [M, K])."""
+    h = np.ascontiguousarray(np.atleast_2d(h), dtype=np.uint16)
+    M, K = h.shape
+    qx = np.empty((M, K), dtype=np.uint8)
+    sx = np.empty(M, dtype=np.float32)
+    _ok(_L().or_fp8_act_quantize(_p(h), M, K, _p(qx), _p(sx)), "fp8_act_quantize")
+    return qx, sx
+
+
 # ---- draft step -----------------------------------------------------------
+
+def gemv_w8a8(q: np.ndarray, scale, qx: np.ndarray, sx: np.ndarray, want_abs: bool = True):
+    """(y float64[M, N], A float64[M, N] or None): W8A8 FP8 logits of every head
+    row from the per-token activation codes qx [M, K] and scales sx [M]."""
+    q = np.ascontiguousarray(q, dtype=np.uint8)
+    qx = np.ascontiguousarray(np.atleast_2d(qx), dtype=np.uint8)
+    sx = np.ascontiguousarray(sx, dtype=np.float32)
+    N, K = q.shape
+    M = qx.shape[0]
+    assert qx.shape[1] == K and sx.size == M
+    y = np.empty((M, N), dtype=np.float64)
+    A = np.empty((M, N), dtype=np.float64) if want_abs else None
+    _ok(_L().or_gemv_w8a8(_p(q), float(scale), N, K, _p(qx), _p(sx), M, _p(y),
+                          _p(A) if want_abs else None), "gemv_w8a8")
+    return y, A
+
 
 def gemv(fmt: int, q: np.ndarray, sf, scale, h: np.ndarray, want_abs: bool = True):
     """(y float64[M, N], A float64[M, N] or None): fp64 logits of every head row."""

@@ -14,7 +14,8 @@
  *         compute_logits (-inf row, index_copy_ of the kept logits).
  *  [FP8]  "FP8 MTP draft stack for vLLM - +6.6% decode on modelopt NVFP4
  *         Qwen3.5-family checkpoints", function _fp8_convert_draft_head
- *         (per-tensor E4M3 head) and Qwen3_5MTP.compute_logits.
+ *         (per-tensor E4M3 head), _Fp8DraftHeadMethod.apply (per-token dynamic
+ *         E4M3 activations, scaled matmul) and Qwen3_5MTP.compute_logits.
  *  [H98K] "Qwen3.8-Flash-Next-ABLITERATED - MTP drafter, NVFP4 experts + 98K FP8
  *         head", section "How it was built": NVFP4 = global scale amax/(6*448),
  *         E4M3 block scales per 16 elements, e2m1 round-to-nearest-even.
@@ -27,7 +28,11 @@
  *  - the NVFP4 amax is clamped below at 1e-12 as the FP8 head's amax is;
  *  - block scale t = bamax / fp32(6*g); element x = w / fp32(dec(s)*g);
  *  - a block whose decoded scale is 0 encodes every element as a signed zero;
- *  - codes are packed two per byte, element 2i in the low nibble.
+ *  - codes are packed two per byte, element 2i in the low nibble;
+ *  - the per-token activation scale is amax_m / 448 with amax_m clamped below
+ *    at 1e-12 and codes E4M3_RNE(clamp(h / s, +-448)), the head's own recipe
+ *    applied per row (the page calls a library quantiser whose code is not on
+ *    the pages).
  */
 #include <math.h>
 #include <stdint.h>
@@ -268,9 +273,74 @@ int or_fp8_quantize(const uint16_t *W, int V, int K, const int32_t *idx, int N,
     return OR_OK;
 }
 
+/* Dynamic per-token FP8 quantisation of the draft hidden states, the
+ * activation half of the W8A8 head [FP8 _Fp8DraftHeadMethod.apply:
+ * scaled_fp8_quant(x, use_per_token_if_dynamic=True) before the scaled
+ * matmul]. Per row m: amax_m = max_k |h[m, k]| clamped below at 1e-12 (as the
+ * head's own amax is), s_m = fp32(amax_m / 448),
+ * qx[m, k] = E4M3_RNE(clamp(fp32(h[m, k] / s_m), +-448)). Same recipe as the
+ * head's per-tensor quantisation, one scale per row. */
+int or_fp8_act_quantize(const uint16_t *h, int M, int K, uint8_t *qx, float *sx)
+{
+    int m, k;
+    if (!h || !qx || !sx || M <= 0 || K <= 0)
+        return OR_ERR_ARG;
+    for (m = 0; m < M; m++) {
+        float amax = 0.0f, s;
+        for (k = 0; k < K; k++) {
+            float a = fabsf(bf16_value(h[(size_t)m * K + k]));
+            if (a > amax)
+                amax = a;
+        }
+        if (amax < 1e-12f)
+            amax = 1e-12f;
+        s = amax / 448.0f;
+        for (k = 0; k < K; k++) {
+            float x = bf16_value(h[(size_t)m * K + k]) / s;
+            if (x > 448.0f)
+                x = 448.0f;
+            if (x < -448.0f)
+                x = -448.0f;
+            qx[(size_t)m * K + k] = (uint8_t)or_e4m3_encode(x);
+        }
+        sx[m] = s;
+    }
+    return OR_OK;
+}
+
 /* ------------------------------------------------------------------------ */
 /* Draft step: GEMV, argmax, id map, logits scatter                         */
 /* ------------------------------------------------------------------------ */
+
+/* W8A8 FP8 head [FP8 _Fp8DraftHeadMethod.apply: cutlass_scaled_mm(qx, W, sx,
+ * weight_scale)]: y[m, n] = scale * sx[m] * sum_k dec(q[n, k]) * dec(qx[m, k]),
+ * in fp64 (every product of two E4M3 values is exact), and A[m, n] the same
+ * sum of |products| (tolerance scale). q row-major [N][K], qx [M][K] as
+ * written by or_fp8_act_quantize. A may be NULL. */
+int or_gemv_w8a8(const uint8_t *q, float scale, int N, int K, const uint8_t *qx,
+                 const float *sx, int M, double *y, double *A)
+{
+    double e4[256];
+    int m, n, k;
+    if (!q || !qx || !sx || !y || N <= 0 || K <= 0 || M <= 0)
+        return OR_ERR_ARG;
+    for (k = 0; k < 256; k++)
+        e4[k] = or_e4m3_decode(k);
+    for (n = 0; n < N; n++)
+        for (m = 0; m < M; m++) {
+            const double ws = (double)scale * (double)sx[m];
+            double s = 0.0, a = 0.0;
+            for (k = 0; k < K; k++) {
+                double p = e4[q[(size_t)n * K + k]] * e4[qx[(size_t)m * K + k]];
+                s += p;
+                a += fabs(p);
+            }
+            y[(size_t)m * N + n] = s * ws;
+            if (A)
+                A[(size_t)m * N + n] = a * fabs(ws);
+        }
+    return OR_OK;
+}
 
 /* y[m, n] = sum_k w'[n, k] * h[m, k] in fp64, and A[m, n] = sum_k |w'[n, k] h[m, k]|
  * (the scale of the logits tolerance) [Q38 get_top_tokens / compute_logits:

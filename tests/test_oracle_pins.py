@@ -275,7 +275,7 @@ def test_fp8_closed_form_and_error_bound(oracle_lib):
     wq = torch_e4m3_values()[q] * float(scale)
     err = np.abs(w.astype(np.float64) - wq)
     assert np.all(err <= np.maximum(2.0 ** -4 * np.abs(w), 2.0 ** -10 * float(scale)) * (1 + 1e-6))
-    assert np.abs(q.view(np.int8)).max() == 0x7E                # amax element -> +-448
+    assert (q & 0x7F).max() == 0x7E                              # amax element -> +-448
 
 
 def test_zero_head_uses_amax_floor(oracle_lib):
@@ -400,3 +400,72 @@ def test_argmax_first_max_and_pads(oracle_lib):
     y, _ = oracle_lib.gemv(oracle_lib.FMT_NVFP4, q, sf, g, hh)
     assert np.array_equal(y[0], y[1])
     assert np.all(y[:, nk:] == y[:, :1])
+
+
+# ------------------------------------------------- W8A8 FP8 head (per-token) ----
+
+def test_fp8_act_quantize_hand_worked_row(oracle_lib):
+    # amax = 448 c, so s = c and every quotient below is exact; E4M3 bytes by
+    # the format (bias 7, 3 mantissa bits): 448 = 1.75 * 2^8 -> 0x7E,
+    # -224 -> 0xF6, 1 -> 0x38, 0 -> 0x00; 17 = 1.0625 * 2^4 lies halfway
+    # between 16 (mantissa 000) and 18 (001) -> even -> 0x58; 19 lies halfway
+    # between 18 (001) and 20 (010) -> even -> 0x5A.
+    vals = np.array([448.0, -224.0, 1.0, 0.0, 17.0, 19.0], np.float32)
+    for c in (1.0, 2.0 ** -3, 2.0 ** 5):
+        qx, sx = oracle_lib.fp8_act_quantize(bf16(vals * np.float32(c))[None])
+        assert [int(v) for v in qx[0]] == [0x7E, 0xF6, 0x38, 0x00, 0x58, 0x5A]
+        assert sx[0] == np.float32(c)
+
+
+def test_fp8_act_quantize_rows_are_independent_and_zero_row_floors(oracle_lib):
+    h = syn.hidden_bf16(40, 3, 64)
+    h[1] = 0
+    qx, sx = oracle_lib.fp8_act_quantize(h)
+    assert sx[1] == np.float32(1e-12) / np.float32(448) and not qx[1].any()
+    for m in (0, 2):
+        q1, s1 = oracle_lib.fp8_act_quantize(h[m:m + 1])
+        assert np.array_equal(q1[0], qx[m]) and s1[0] == sx[m]
+        x = syn.bf16_bits_to_f32(h[m])
+        assert sx[m] == np.float32(np.abs(x).max()) / np.float32(448)
+
+
+def test_fp8_act_quantize_error_bound_against_torch_values(oracle_lib):
+    h = syn.hidden_bf16(41, 4, 256)
+    qx, sx = oracle_lib.fp8_act_quantize(h)
+    x = syn.bf16_bits_to_f32(h).astype(np.float64)
+    xq = torch_e4m3_values()[qx] * sx[:, None].astype(np.float64)
+    bound = np.maximum(2.0 ** -4 * np.abs(x), 2.0 ** -10 * sx[:, None].astype(np.float64))
+    assert np.all(np.abs(x - xq) <= bound * (1 + 1e-6))
+    assert np.all((qx & 0x7F).max(axis=1) == 0x7E)                # each row's amax -> +-448
+
+
+def test_w8a8_reduces_to_w8a16_when_h_is_on_the_e4m3_grid(oracle_lib):
+    # h = 2^-3 * (E4M3 values with a 448 in every row): per-token quantisation
+    # is then exact (s = 2^-3), so the W8A8 logits equal the W8A16 logits of the
+    # same head, computed by the separately pinned or_gemv.
+    rng = np.random.default_rng(42)
+    e4 = torch_e4m3_values()
+    finite = np.array([b for b in range(256) if np.isfinite(e4[b])])
+    K, M = 128, 3
+    codes = rng.choice(finite, size=(M, K))
+    codes[:, 7] = 0x7E
+    h = bf16((e4[codes] * 2.0 ** -3).astype(np.float32))
+    W, keep, _ = _tiny_case(43, K=K)
+    idx, _ = oracle_lib.build_index(keep)
+    q, s = oracle_lib.fp8_quantize(W, idx)
+    qx, sx = oracle_lib.fp8_act_quantize(h)
+    assert np.array_equal(qx, codes) and np.all(sx == np.float32(2.0 ** -3))
+    y8, A8 = oracle_lib.gemv_w8a8(q, s, qx, sx)
+    y16, A16 = oracle_lib.gemv(oracle_lib.FMT_FP8, q, None, s, h)
+    assert np.allclose(y8, y16, rtol=1e-13, atol=1e-15) and np.allclose(A8, A16, rtol=1e-13)
+
+
+def test_w8a8_matches_numpy_on_decoded_codes(oracle_lib):
+    W, keep, h = _tiny_case(44)
+    idx, _ = oracle_lib.build_index(keep)
+    q, s = oracle_lib.fp8_quantize(W, idx)
+    qx, sx = oracle_lib.fp8_act_quantize(h)
+    y, _ = oracle_lib.gemv_w8a8(q, s, qx, sx)
+    e4 = torch_e4m3_values()
+    ref = (e4[qx] @ e4[q].T) * float(s) * sx[:, None].astype(np.float64)
+    assert np.allclose(y, ref, rtol=1e-12, atol=1e-14)
