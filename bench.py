@@ -460,7 +460,18 @@ def run_suite(args):
         line(f"fp8 98,304 top_tokens M={M}", graph_us(calls), fb + M * (2 * K_HID + 4), {"M": M})
         calls = [(lambda i=i: h8s[i % 3].compute_logits(hsM[i % 8, :M], out=out)) for i in range(steps)]
         line(f"fp8 98,304 compute_logits M={M}", graph_us(calls), fb + M * (2 * K_HID + 4 * 248_320), {"M": M})
-    del h8s, h8
+    # the same head run W8A8 (per-token FP8 hidden states quantised inside the step)
+    w8 = [dh.DraftHead(dh.DH_FMT_FP8_W8A8, x.V, x.q, x.idx, x.n_kept, scale=x.scale, idx_ascending=True)
+          for x in h8s]
+    for M in (1, 4, 16):
+        ids = torch.empty(M, dtype=torch.int32, device=dev)
+        out = torch.empty((M, 248_320), dtype=torch.float32, device=dev)
+        calls = [(lambda i=i: w8[i % 3].top_tokens(hsM[i % 8, :M], ids=ids)) for i in range(steps)]
+        line(f"fp8 w8a8 98,304 top_tokens M={M}", graph_us(calls), fb + M * (2 * K_HID + 4), {"M": M})
+        calls = [(lambda i=i: w8[i % 3].compute_logits(hsM[i % 8, :M], out=out)) for i in range(steps)]
+        line(f"fp8 w8a8 98,304 compute_logits M={M}", graph_us(calls), fb + M * (2 * K_HID + 4 * 248_320),
+             {"M": M})
+    del h8s, h8, w8
 
     # BF16 full-vocabulary head, the stock drafter read (1.27 GB > L2)
     hf = dh.bf16_full_head(Wd)

@@ -68,7 +68,13 @@ typedef enum {
 #define DH_DEVERR_IDX 1u      /* a dh_idx entry was outside [0, V) */
 #define DH_DEVERR_TIMEOUT 2u  /* a bounded device wait gave up (results invalid) */
 
-typedef enum { DH_FMT_NVFP4 = 1, DH_FMT_FP8 = 2, DH_FMT_BF16 = 3, DH_FMT_NVFP4_PACKED = 4 } dh_format;
+typedef enum {
+    DH_FMT_NVFP4 = 1,
+    DH_FMT_FP8 = 2,
+    DH_FMT_BF16 = 3,
+    DH_FMT_NVFP4_PACKED = 4,
+    DH_FMT_FP8_W8A8 = 5
+} dh_format;
 
 /* A quantised draft head. Plain descriptor: the library never owns these.
  *   fmt     DH_FMT_NVFP4: q = E2M1 codes [N][K/2], element 2i of a row in the
@@ -82,6 +88,12 @@ typedef enum { DH_FMT_NVFP4 = 1, DH_FMT_FP8 = 2, DH_FMT_BF16 = 3, DH_FMT_NVFP4_P
  *                         tile-major bytes (N * (K/2 + K/16)); sf = NULL;
  *                         scale = &g. Same values, the layout the draft-step
  *                         kernel streams fastest.
+ *           DH_FMT_FP8_W8A8: the FP8 head (q, scale as for DH_FMT_FP8) run
+ *                         W8A8 ("FP8 MTP draft stack ...",
+ *                         _Fp8DraftHeadMethod.apply): each draft step first
+ *                         quantises every hidden row to E4M3 with its own
+ *                         scale (as fp8_quantize_activations does) and then
+ *                         y[m, n] = scale * sx[m] * sum_k q[n, k] * qx[m, k].
  *   V       target vocabulary size (width of the compute_logits rows).
  *   K       hidden size. Supported by the draft-step kernels: 256, 2560
  *           (the pages' drafter hidden size) and 5120.
@@ -146,6 +158,17 @@ int nvfp4_quantize_rows(const void *W, int V, int K, const int32_t *idx, int N,
  * Arguments as for nvfp4_quantize_rows. */
 int fp8_quantize_rows(const void *W, int V, int K, const int32_t *idx, int N,
                       uint8_t *q, float *scale, void *ws, size_t ws_bytes, void *stream);
+
+/* Per-token dynamic FP8 quantisation of hidden states, the activation half of
+ * the W8A8 head ("FP8 MTP draft stack ...", _Fp8DraftHeadMethod.apply:
+ * scaled_fp8_quant with one scale per token). For each row m < M:
+ *   sx[m] = max(max_k |h[m, k]|, 1e-12) / 448   (fp32, IEEE division),
+ *   qx[m, k] = E4M3_RNE(clamp(h[m, k] / sx[m], +-448)).
+ *   h  BF16 [M][K] row-major, 16-byte aligned; qx out E4M3 codes [M][K],
+ *      16-byte aligned; sx out float [M]. M >= 1, K % 16 == 0.
+ * One kernel on `stream`; the W8A8 draft step computes the same codes
+ * internally, so this call serves callers that want the codes themselves. */
+int fp8_quantize_activations(const void *h, int M, int K, uint8_t *qx, float *sx, void *stream);
 
 /* Repack an NVFP4 head into the tile-major layout of DH_FMT_NVFP4_PACKED,
  * the layout Marlin-style GEMV kernels also use instead of the quantiser's
@@ -212,6 +235,11 @@ const char *draft_head_status_string(int status);
 
 /* DH_ABI_VERSION of the loaded library. */
 int draft_head_abi_version(void);
+
+/* The cudaError_t of the CUDA call or launch behind the calling thread's most
+ * recent DH_ERR_CUDA (0 before any). If name is not NULL, *name points to the
+ * error's static name (cudaGetErrorName). Host only; never touches the GPU. */
+int draft_head_last_cuda_error(const char **name);
 
 #ifdef __cplusplus
 }

@@ -8,6 +8,7 @@ Names follow the C ABI in include/drafthead.h:
   draft_head_build_index   keep mask -> dh_idx (padded to N % 64 == 0)
   nvfp4_quantize_rows      gather + NVFP4 quantisation of W[dh_idx]
   fp8_quantize_rows        gather + per-tensor FP8 E4M3 quantisation
+  fp8_quantize_activations per-token FP8 E4M3 codes of hidden states (W8A8)
   DraftHead.top_tokens     get_top_tokens: dh_idx[argmax_n (W_q h)]
   DraftHead.compute_logits compute_logits: -inf row + logits at dh_idx
 """
@@ -22,7 +23,7 @@ import torch
 from . import build as _build
 
 DH_OK, DH_ERR_ARG, DH_ERR_SHAPE, DH_ERR_ALIGN, DH_ERR_WORKSPACE, DH_ERR_CUDA = 0, 1, 2, 3, 4, 5
-DH_FMT_NVFP4, DH_FMT_FP8, DH_FMT_BF16, DH_FMT_NVFP4_PACKED = 1, 2, 3, 4
+DH_FMT_NVFP4, DH_FMT_FP8, DH_FMT_BF16, DH_FMT_NVFP4_PACKED, DH_FMT_FP8_W8A8 = 1, 2, 3, 4, 5
 DH_MAX_M = 16
 DH_WORKSPACE_ALIGN = 256
 DH_DEVERR_IDX = 1
@@ -34,7 +35,7 @@ EXPORTS = (
     "fp8_quantize_rows", "draft_head_workspace_bytes", "draft_head_workspace_init",
     "draft_head_top_tokens", "draft_head_compute_logits", "draft_head_read_device_error",
     "draft_head_status_string", "draft_head_abi_version", "draft_head_top_tokens_static",
-    "nvfp4_pack_head",
+    "nvfp4_pack_head", "fp8_quantize_activations", "draft_head_last_cuda_error",
 )
 
 _lib = None
@@ -43,6 +44,11 @@ _lib = None
 class DraftHeadError(RuntimeError):
     def __init__(self, fn: str, status: int):
         msg = lib().draft_head_status_string(status).decode() if _lib is not None else str(status)
+        self.cuda_error = 0
+        if status == DH_ERR_CUDA and _lib is not None:
+            name = C.c_char_p()
+            self.cuda_error = _lib.draft_head_last_cuda_error(C.byref(name))
+            msg += f": {name.value.decode() if name.value else self.cuda_error}"
         super().__init__(f"{fn}: status {status} ({msg})")
         self.status = status
 
@@ -83,6 +89,8 @@ def lib():
         L.draft_head_abi_version.argtypes = []
         L.draft_head_top_tokens_static.argtypes = [C.POINTER(dh_head_t), P, I, P, P, P]
         L.nvfp4_pack_head.argtypes = [P, P, I, I, P, P]
+        L.fp8_quantize_activations.argtypes = [P, I, I, P, P, P]
+        L.draft_head_last_cuda_error.argtypes = [C.POINTER(C.c_char_p)]
         _lib = L
     return _lib
 
@@ -171,6 +179,19 @@ def nvfp4_pack_head(q: torch.Tensor, sf: torch.Tensor, stream=None) -> torch.Ten
     return packed
 
 
+def fp8_quantize_activations(h: torch.Tensor, stream=None):
+    """(qx uint8[M, K] E4M3 codes, sx float32[M] scales): per-token dynamic FP8
+    quantisation of BF16 hidden states, as the W8A8 head's draft step does it."""
+    if h.dtype != torch.bfloat16 or h.dim() != 2 or not h.is_cuda or not h.is_contiguous():
+        raise ValueError("h must be a contiguous [M, K] bfloat16 CUDA tensor")
+    M, K = h.shape
+    qx = torch.empty((M, K), dtype=torch.uint8, device=h.device)
+    sx = torch.empty(M, dtype=torch.float32, device=h.device)
+    _check("fp8_quantize_activations",
+           lib().fp8_quantize_activations(h.data_ptr(), M, K, qx.data_ptr(), sx.data_ptr(), _stream(stream)))
+    return qx, sx
+
+
 def draft_head_read_device_error(ws: torch.Tensor, stream=None) -> int:
     err = C.c_int()
     _check("draft_head_read_device_error",
@@ -189,8 +210,9 @@ def _raise_device_error(ws, stream, fn):
 class DraftHead:
     """A quantised draft head plus its workspace; tensors stay owned by torch.
 
-    fmt: DH_FMT_NVFP4 (q, sf, scale=g), DH_FMT_FP8 (q, scale) or DH_FMT_BF16 (q =
-    the BF16 weights, idx may be None for a full-vocabulary head).
+    fmt: DH_FMT_NVFP4 (q, sf, scale=g), DH_FMT_NVFP4_PACKED (tile-major q, scale=g),
+    DH_FMT_FP8 / DH_FMT_FP8_W8A8 (q, scale) or DH_FMT_BF16 (q = the BF16
+    weights, idx may be None for a full-vocabulary head).
     """
 
     def __init__(self, fmt: int, V: int, q: torch.Tensor, idx: torch.Tensor | None, n_kept: int,
@@ -205,7 +227,7 @@ class DraftHead:
             self.K = q.shape[1] * 128
         elif fmt == DH_FMT_NVFP4:
             self.K = q.shape[1] * 2
-        elif fmt == DH_FMT_FP8:
+        elif fmt in (DH_FMT_FP8, DH_FMT_FP8_W8A8):
             self.K = q.shape[1]
         else:
             self.K = q.shape[1] if q.dtype == torch.bfloat16 else q.shape[1] // 2
@@ -269,12 +291,14 @@ def nvfp4_head(W: torch.Tensor, keep, packed: bool = True, stream=None) -> Draft
     return DraftHead(DH_FMT_NVFP4, W.shape[0], q, idx, nk, sf=sf, scale=g, idx_ascending=True)
 
 
-def fp8_head(W: torch.Tensor, keep, stream=None) -> DraftHead:
-    """Build a per-tensor FP8 draft head from a BF16 target head and a host keep mask."""
+def fp8_head(W: torch.Tensor, keep, w8a8: bool = False, stream=None) -> DraftHead:
+    """Build a per-tensor FP8 draft head from a BF16 target head and a host keep
+    mask: W8A16 (BF16 hidden states), or W8A8 (per-token FP8 hidden states)."""
     idx_np, nk = draft_head_build_index(keep)
     idx = torch.from_numpy(idx_np).to(W.device)
     q, s = fp8_quantize_rows(W, idx, stream)
-    return DraftHead(DH_FMT_FP8, W.shape[0], q, idx, nk, scale=s, idx_ascending=True)
+    return DraftHead(DH_FMT_FP8_W8A8 if w8a8 else DH_FMT_FP8, W.shape[0], q, idx, nk, scale=s,
+                     idx_ascending=True)
 
 
 def bf16_full_head(W: torch.Tensor) -> DraftHead:

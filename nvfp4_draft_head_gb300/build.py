@@ -19,10 +19,14 @@ OUT_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(OUT_DIR, "libdrafthead.so")
 
 SOURCES = ["dh_abi.cu", "dh_quantize.cu", "dh_gemv.cu", "dh_gemv_nvfp4.cu", "dh_gemv_fp8.cu",
-           "dh_gemv_bf16.cu", "dh_static_ws.cu", "dh_gemv_nvfp4p.cu", "dh_pack.cu"]
+           "dh_gemv_bf16.cu", "dh_static_ws.cu", "dh_gemv_nvfp4p.cu", "dh_pack.cu",
+           "dh_gemv_w8a8.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-NVCC_FLAGS = ["-std=c++17", "-O3", "-lineinfo", "-Xcompiler", "-fPIC", "-I", INCLUDE,
-              "--expt-relaxed-constexpr"]
+# -fno-gnu-unique: the launchers' per-device caches (function-local statics of
+# templates) stay private to each loaded copy of the library instead of being
+# merged process-wide, so two builds loaded side by side do not share them.
+NVCC_FLAGS = ["-std=c++17", "-O3", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fno-gnu-unique",
+              "-I", INCLUDE, "--expt-relaxed-constexpr"]
 
 
 def nvcc() -> str:

@@ -12,7 +12,14 @@ namespace {
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-int cuda_status(cudaError_t e) { return e == cudaSuccess ? DH_OK : DH_ERR_CUDA; }
+// cudaError_t behind the calling thread's last DH_ERR_CUDA (0 if none yet).
+thread_local int t_last_cuda_error = 0;
+
+int cuda_status(cudaError_t e) {
+    if (e == cudaSuccess) return DH_OK;
+    t_last_cuda_error = static_cast<int>(e);
+    return DH_ERR_CUDA;
+}
 
 int check_ws(const void* ws, size_t ws_bytes, size_t need) {
     if (ws == nullptr) return DH_ERR_ARG;
@@ -31,13 +38,16 @@ int check_gather(const void* W, int V, int K, const int32_t* idx, int N) {
 
 int check_head(const dh_head_t* hd) {
     if (hd == nullptr || hd->q == nullptr) return DH_ERR_ARG;
-    if (hd->fmt != DH_FMT_NVFP4 && hd->fmt != DH_FMT_FP8 && hd->fmt != DH_FMT_BF16 && hd->fmt != DH_FMT_NVFP4_PACKED)
+    if (hd->fmt != DH_FMT_NVFP4 && hd->fmt != DH_FMT_FP8 && hd->fmt != DH_FMT_BF16 && hd->fmt != DH_FMT_NVFP4_PACKED &&
+        hd->fmt != DH_FMT_FP8_W8A8)
         return DH_ERR_ARG;
     if (hd->V <= 0 || hd->N <= 0 || hd->n_kept < 1 || hd->n_kept > hd->N) return DH_ERR_SHAPE;
     if (hd->N % 64 != 0) return DH_ERR_SHAPE;
     if (!dh::gemv_supported(hd->fmt, hd->K)) return DH_ERR_SHAPE;
     if (hd->fmt == DH_FMT_NVFP4 && (hd->sf == nullptr || hd->scale == nullptr)) return DH_ERR_ARG;
-    if ((hd->fmt == DH_FMT_FP8 || hd->fmt == DH_FMT_NVFP4_PACKED) && hd->scale == nullptr) return DH_ERR_ARG;
+    if ((hd->fmt == DH_FMT_FP8 || hd->fmt == DH_FMT_NVFP4_PACKED || hd->fmt == DH_FMT_FP8_W8A8) &&
+        hd->scale == nullptr)
+        return DH_ERR_ARG;
     if (hd->idx == nullptr) {
         if (hd->fmt != DH_FMT_BF16) return DH_ERR_ARG;
         if (hd->n_kept != hd->N || hd->N > hd->V) return DH_ERR_SHAPE;
@@ -80,6 +90,11 @@ dh::GemvArgs make_args(const dh_head_t* hd, const void* h, int M, void* ws) {
 extern "C" {
 
 int draft_head_abi_version(void) { return DH_ABI_VERSION; }
+
+int draft_head_last_cuda_error(const char** name) {
+    if (name != nullptr) *name = cudaGetErrorName(static_cast<cudaError_t>(t_last_cuda_error));
+    return t_last_cuda_error;
+}
 
 const char* draft_head_status_string(int status) {
     switch (status) {
@@ -140,6 +155,15 @@ int fp8_quantize_rows(const void* W, int V, int K, const int32_t* idx, int N, ui
                                                static_cast<cudaStream_t>(stream)));
 }
 
+int fp8_quantize_activations(const void* h, int M, int K, uint8_t* qx, float* sx, void* stream) {
+    if (h == nullptr || qx == nullptr || sx == nullptr) return DH_ERR_ARG;
+    if (M < 1 || K <= 0 || K % 16 != 0) return DH_ERR_SHAPE;
+    if (static_cast<long long>(M) * K >= (1ll << 40) || M > 65535) return DH_ERR_SHAPE;
+    if (!aligned(h, 16) || !aligned(qx, 16) || !aligned(sx, 4)) return DH_ERR_ALIGN;
+    return cuda_status(dh::launch_fp8_act_quantize(static_cast<const uint16_t*>(h), M, K, qx, sx,
+                                                   static_cast<cudaStream_t>(stream)));
+}
+
 int nvfp4_pack_head(const uint8_t* q, const uint8_t* sf, int N, int K, uint8_t* packed, void* stream) {
     if (q == nullptr || sf == nullptr || packed == nullptr) return DH_ERR_ARG;
     if (N <= 0 || K <= 0 || N % 16 != 0 || K % 128 != 0) return DH_ERR_SHAPE;
@@ -184,7 +208,7 @@ int draft_head_compute_logits(const dh_head_t* hd, const void* h, int M, float* 
     dh::GemvArgs a = make_args(hd, h, M, ws);
     a.out = out;
     cudaError_t e = dh::launch_fill_neg_inf(out, static_cast<size_t>(M) * hd->V, s);
-    if (e != cudaSuccess) return DH_ERR_CUDA;
+    if (e != cudaSuccess) return cuda_status(e);
     return cuda_status(dh::launch_gemv(a, s));
 }
 
@@ -194,9 +218,10 @@ int draft_head_read_device_error(void* ws, int* err, void* stream) {
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     dh::Workspace* w = static_cast<dh::Workspace*>(ws);
     unsigned int v = 0;
-    if (cudaMemcpyAsync(&v, &w->error, sizeof v, cudaMemcpyDeviceToHost, s) != cudaSuccess) return DH_ERR_CUDA;
-    if (cudaMemsetAsync(&w->error, 0, sizeof v, s) != cudaSuccess) return DH_ERR_CUDA;
-    if (cudaStreamSynchronize(s) != cudaSuccess) return DH_ERR_CUDA;
+    cudaError_t e = cudaMemcpyAsync(&v, &w->error, sizeof v, cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(&w->error, 0, sizeof v, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_status(e);
     *err = static_cast<int>(v);
     return DH_OK;
 }

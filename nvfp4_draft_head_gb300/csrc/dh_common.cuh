@@ -5,6 +5,7 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 #include <cuda_fp16.h>
+#include <cuda_fp8.h>
 
 namespace dh {
 
@@ -107,6 +108,22 @@ __device__ __forceinline__ float fma2_bf16_f32(uint32_t a, uint32_t b, float acc
     return acc;
 }
 
+// Per-token dynamic FP8 quantisation of hidden states, the activation half of
+// the W8A8 head ("FP8 MTP draft stack for vLLM ...", _Fp8DraftHeadMethod.apply:
+// scaled_fp8_quant(x, use_per_token_if_dynamic=True)). A row's scale is its
+// max |h| clamped below at 1e-12, divided by 448 (IEEE division).
+__device__ __forceinline__ float act_fp8_scale(float amax) {
+    return __fdiv_rn(amax < 1e-12f ? 1e-12f : amax, 448.0f);
+}
+
+// E4M3 codes of the two BF16 values of w (low half -> low byte):
+// E4M3_RNE(clamp(h / s, +-448)), the division IEEE round-to-nearest.
+__device__ __forceinline__ uint32_t act_fp8_pair(uint32_t w, float s) {
+    const float lo = fminf(fmaxf(__fdiv_rn(bf16_lo(w), s), -448.0f), 448.0f);
+    const float hi = fminf(fmaxf(__fdiv_rn(bf16_hi(w), s), -448.0f), 448.0f);
+    return static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(make_float2(lo, hi), __NV_SATFINITE, __NV_E4M3));
+}
+
 // Power of two 2^e with e clamped to the normal float range.
 __device__ __forceinline__ float exp2i(int e) {
     e = e < -126 ? -126 : (e > 127 ? 127 : e);
@@ -189,6 +206,16 @@ __device__ __forceinline__ void cp_async16(void* dst, const void* src) {
 
 __device__ __forceinline__ void cp_async_wait_all() {
     asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
+__device__ __forceinline__ void cp_async_commit() {
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+
+// Wait until at most N of this thread's committed cp.async groups are pending.
+template <int N>
+__device__ __forceinline__ void cp_async_wait_group() {
+    asm volatile("cp.async.wait_group %0;" :: "n"(N) : "memory");
 }
 
 // L2 policy for data read once per step (the head): evict first.

@@ -10,6 +10,7 @@ cudaError_t launch_gemv_nvfp4(const GemvArgs& a, cudaStream_t s);
 cudaError_t launch_gemv_fp8(const GemvArgs& a, cudaStream_t s);
 cudaError_t launch_gemv_bf16(const GemvArgs& a, cudaStream_t s);
 cudaError_t launch_gemv_nvfp4_packed(const GemvArgs& a, cudaStream_t s);
+cudaError_t launch_gemv_fp8_w8a8(const GemvArgs& a, cudaStream_t s);
 
 __global__ void fill_neg_inf_kernel(float4* out4, size_t n4, float* tail, int ntail) {
     const float ninf = __uint_as_float(0xFF800000u);
@@ -35,7 +36,7 @@ int sm_count() {
 #define DH_GEMV_KS(X) X(256) X(2560) X(5120)
 
 bool gemv_supported(int fmt, int K) {
-    if (fmt < 1 || fmt > 4) return false;
+    if (fmt < 1 || fmt > 5) return false;
 #define DH_CASE(k) if (K == k) return true;
     DH_GEMV_KS(DH_CASE)
 #undef DH_CASE
@@ -47,6 +48,7 @@ cudaError_t launch_gemv(const GemvArgs& a, cudaStream_t s) {
     if (a.fmt == 1) return launch_gemv_nvfp4(a, s);
     if (a.fmt == 2) return launch_gemv_fp8(a, s);
     if (a.fmt == 4) return launch_gemv_nvfp4_packed(a, s);
+    if (a.fmt == 5) return launch_gemv_fp8_w8a8(a, s);
     return launch_gemv_bf16(a, s);
 }
 

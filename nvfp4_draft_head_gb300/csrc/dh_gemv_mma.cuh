@@ -33,6 +33,15 @@
 // With several drafts (and for FP8 / BF16) the 8 columns are drafts: the NVFP4
 // codes are multiplied by their block scale in f16 first (exact: at most 6
 // significant bits, magnitude at most 2688), and D accumulates over all k.
+//
+// W8A8 FP8 head ("FP8 MTP draft stack for vLLM ...", _Fp8DraftHeadMethod.apply:
+// per-token dynamic E4M3 activations, scaled FP8 matmul). The compute warps
+// quantise h themselves: each finds the max |h| of its windows per draft, the
+// CTA's compute warps combine them in shared memory, and every thread encodes
+// its own 32 k of each draft (the codes are the B fragments). The multiply-adds
+// are mma.sync m16n8k32 e4m3 x e4m3 -> f32 on the raw codes (products of two
+// E4M3 values are exact in f32); a draft's partials are scaled by its
+// activation scale, the reducer's sum by the head's scale.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -44,6 +53,10 @@
 
 namespace dh {
 namespace mma {
+
+#ifndef DH_RING_STAGES
+#define DH_RING_STAGES 0  // packed NVFP4: cp.async shared-memory stages per compute warp (0: register loads)
+#endif
 
 constexpr int cmin(int a, int b) { return a < b ? a : b; }
 constexpr int cmax(int a, int b) { return a > b ? a : b; }
@@ -62,7 +75,8 @@ struct Cfg {
     static constexpr bool NV = (FMT == 1 || FMT == 4);       // NVFP4 (canonical or packed layout)
     static constexpr bool PACKED = (FMT == 4);                // tile-major NVFP4 layout
     static constexpr bool BLOCKDIAG = (NV && MT == 1);
-    static constexpr int BPE2 = NV ? 1 : (FMT == 2 ? 2 : 4);  // bytes per 2 elements
+    static constexpr bool W8A8 = (FMT == 5);                  // FP8 head, FP8 activations
+    static constexpr int BPE2 = NV ? 1 : ((FMT == 2 || W8A8) ? 2 : 4);  // bytes per 2 elements
     static constexpr int RB = K * BPE2 / 2;                   // code bytes per head row
     static constexpr int WB = 128 * BPE2 / 2;                 // code bytes per row and window
     static constexpr int CPR = WB / 4 / 16;                   // 16-byte loads per row, window, thread
@@ -72,7 +86,16 @@ struct Cfg {
     // register loads in flight (tiles ahead) when the code bytes come straight to
     // registers; two at 16 drafts, where the h fragments of two n8 tiles leave no
     // room for a third within the 80 registers 21+ warps per SM allow
-    static constexpr int P = cmax(1, cmin(MT >= 16 ? 2 : 3, 48 / TILE_REGS));
+    // Packed NVFP4 with a shared-memory ring: each compute warp keeps RING tiles
+    // of its windows in flight as 16-byte cp.async copies (no registers held),
+    // within ~184 KB of shared memory (~140 KB at 16 drafts, whose partial-sum
+    // ring is larger).
+    static constexpr int RSTAGE = WPW * (16 * 64 + 16 * 8);  // bytes of one warp's stage
+    static constexpr int RING =
+        (PACKED && DH_RING_STAGES > 0)
+            ? cmax(2, cmin(DH_RING_STAGES, (MT >= 16 ? 140 * 1024 : 184 * 1024) / (NW * RSTAGE)))
+            : 0;
+    static constexpr int P = RING > 0 ? 1 : cmax(1, cmin(MT >= 16 ? 2 : 3, 48 / TILE_REGS));
     // Canonical NVFP4 layout: a loader warp streams each tile's scale bytes
     // into a shared-memory ring with 1-D bulk copies.
     static constexpr bool SCALES = (FMT == 1);
@@ -99,6 +122,15 @@ __device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1,
 __device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                          uint32_t b0, uint32_t b1) {
     asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// D += A B with E4M3 A (16 x 32, row) and B (32 x 8, col), f32 accumulation.
+__device__ __forceinline__ void mma_e4m3(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+    asm("mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
         "{%0,%1,%2,%3};"
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
@@ -151,6 +183,33 @@ __device__ __forceinline__ void load_tile(TileBuf<FMT, K, MT>& b, const uint8_t*
     }
 }
 
+// Ring mode: one warp copies its windows' blocks of a tile into a stage.
+template <int FMT, int K, int MT>
+__device__ __forceinline__ void issue_stage(uint8_t* stage, const uint8_t* q, int tile, int warp, int lane) {
+    using C = Cfg<FMT, K, MT>;
+#pragma unroll
+    for (int ww = 0; ww < C::WPW; ++ww) {
+        const uint8_t* src = q + (static_cast<size_t>(tile) * C::NWIN + warp + ww * C::NW) * C::WBLK;
+        uint8_t* dst = stage + ww * C::WBLK;
+        for (int c = lane; c < C::WBLK / 16; c += 32) cp_async16(dst + 16 * c, src + 16 * c);
+    }
+}
+
+// Ring mode: this thread's fragments of a staged tile (same layout as load_tile's).
+template <int FMT, int K, int MT>
+__device__ __forceinline__ void fetch_stage(TileBuf<FMT, K, MT>& b, const uint8_t* stage, int g, int t) {
+    using C = Cfg<FMT, K, MT>;
+#pragma unroll
+    for (int ww = 0; ww < C::WPW; ++ww) {
+        const uint8_t* st = stage + ww * C::WBLK;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            b.c[ww][h][0] = *reinterpret_cast<const uint4*>(st + (g + 8 * h) * 64 + 16 * t);
+            b.s[ww][h] = *reinterpret_cast<const uint2*>(st + 16 * 64 + (g + 8 * h) * 8);
+        }
+    }
+}
+
 // Byte i (0..15) of a 16-byte piece.
 __device__ __forceinline__ uint32_t byte_of(const uint4& v, int i) {
     const uint32_t w = i < 4 ? v.x : (i < 8 ? v.y : (i < 12 ? v.z : v.w));
@@ -185,6 +244,7 @@ __global__ void __launch_bounds__(Cfg<FMT, K, MT>::THREADS, 1) gemv_mma_kernel(c
     __shared__ unsigned long long s_best[NRED];
     __shared__ unsigned long long s_cta[MT];
     __shared__ int s_abort;
+    __shared__ float s_amx[C::W8A8 ? NW : 1][16];  // W8A8: per compute warp and draft, max |h|
     // dh_idx of this CTA's first kIdCap tiles: [i][0..15] the rows' ids, [i][16]
     // the id of the row after the tile (copied when that row exists)
     __shared__ __align__(16) int s_ids[kIdCap * 20];
@@ -197,13 +257,24 @@ __global__ void __launch_bounds__(Cfg<FMT, K, MT>::THREADS, 1) gemv_mma_kernel(c
     const uint8_t* q = static_cast<const uint8_t*>(a.q);
     volatile int* abort_flag = &s_abort;
 
-    // Issue the first P tiles' loads before anything else (compute warps).
+    // Issue the first P tiles' loads (ring mode: the first RING tiles' copies)
+    // before anything else (compute warps).
     TileBuf<FMT, K, MT> buf[P];
+    uint8_t* ring = s_scales + ((C::RING > 0 && warp < NW) ? warp * C::RING * C::RSTAGE : 0);  // this warp's stages
     if (warp < NW) {
+        if constexpr (C::RING > 0) {
+#pragma unroll 1
+            for (int i = 0; i < C::RING; ++i) {
+                if (i < my_tiles) issue_stage<FMT, K, MT>(ring + i * C::RSTAGE, q, blockIdx.x + i * gridDim.x, warp, lane);
+                cp_async_commit();
+            }
+        } else {
 #pragma unroll
-        for (int p = 0; p < P; ++p)
-            if (p < my_tiles) load_tile<FMT, K, MT>(buf[p], q, blockIdx.x + p * gridDim.x, warp, g, t);
+            for (int p = 0; p < P; ++p)
+                if (p < my_tiles) load_tile<FMT, K, MT>(buf[p], q, blockIdx.x + p * gridDim.x, warp, g, t);
+        }
     }
+
     if (tid == 0) {
         for (int r = 0; r < RS; ++r) {
             mbar_init(&full_p[r], NW);
@@ -364,9 +435,48 @@ __global__ void __launch_bounds__(Cfg<FMT, K, MT>::THREADS, 1) gemv_mma_kernel(c
         // BF16 value converts to f16 exactly; the warp's partial logits are
         // scaled back by 2^-e before they leave it.
         uint32_t hb[WPW][NT][16];
-        float unscale[NT][2];  // 2^-e of the drafts of this thread's D columns
+        float unscale[NT][2];  // 2^-e (W8A8: the activation scale) of the drafts of this thread's D columns
+        if constexpr (C::W8A8) {
+            // Per-token E4M3 codes of h: row max over the CTA's compute warps, then
+            // word j of hb[ww][nt] = the codes of k0 + 4j .. k0 + 4j + 3.
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
+            for (int nt = 0; nt < NT; ++nt) {
+                const int d = g + 8 * nt;
+                const bool live = d < a.M;
+                float am = 0.0f;
+#pragma unroll
+                for (int ww = 0; ww < WPW; ++ww) {
+                    const int k0 = 128 * (warp + ww * NW) + 32 * t;
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const uint32_t w = live ? __ldg(h32 + d * KW + k0 / 2 + j) : 0u;
+                        hb[ww][nt][j] = w;
+                        am = fmaxf(am, fmaxf(fabsf(bf16_lo(w)), fabsf(bf16_hi(w))));
+                    }
+                }
+                am = fmaxf(am, __shfl_xor_sync(0xFFFFFFFFu, am, 1));
+                am = fmaxf(am, __shfl_xor_sync(0xFFFFFFFFu, am, 2));
+                if (t == 0) s_amx[warp][d] = am;
+            }
+            named_bar_sync(2, NW * 32);  // compute warps only
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                const int d = g + 8 * nt;
+                float am = 0.0f;
+                for (int w2 = 0; w2 < NW; ++w2) am = fmaxf(am, s_amx[w2][d]);
+                const float sx = act_fp8_scale(am);
+#pragma unroll
+                for (int ww = 0; ww < WPW; ++ww)
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        hb[ww][nt][j] = act_fp8_pair(hb[ww][nt][2 * j], sx) |
+                                        (act_fp8_pair(hb[ww][nt][2 * j + 1], sx) << 16);
+                unscale[nt][0] = __shfl_sync(0xFFFFFFFFu, sx, 4 * (2 * t));
+                unscale[nt][1] = __shfl_sync(0xFFFFFFFFu, sx, 4 * (2 * t + 1));
+            }
+        }
+#pragma unroll
+        for (int nt = 0; nt < (C::W8A8 ? 0 : NT); ++nt) {
             const int d = C::BLOCKDIAG ? 0 : g + 8 * nt;
             const bool live = d < a.M;
             float am = 0.0f;
@@ -430,6 +540,13 @@ __global__ void __launch_bounds__(Cfg<FMT, K, MT>::THREADS, 1) gemv_mma_kernel(c
                 if (ti >= my_tiles) break;
                 TileBuf<FMT, K, MT>& b = buf[p];
                 const int slot = ti % RS;
+                if constexpr (C::RING > 0) {
+                    // tile ti's copies are the oldest group but RING - 1; every lane's
+                    // copies have landed once all lanes passed the wait
+                    cp_async_wait_group<C::RING - 1>();
+                    __syncwarp();
+                    fetch_stage<FMT, K, MT>(b, ring + (ti % C::RING) * C::RSTAGE, g, t);
+                }
                 if constexpr (C::SCALES) {
                     const int ss = ti % C::SS;
                     if (!*abort_flag && !mbar_wait(&full_s[ss], (ti / C::SS) & 1)) {
@@ -491,8 +608,24 @@ __global__ void __launch_bounds__(Cfg<FMT, K, MT>::THREADS, 1) gemv_mma_kernel(c
                     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
                         for (int c = 0; c < 4; ++c) out[nt][c] = 0.0f;
+                    if constexpr (C::W8A8) {
+                        // MMA i: A words 2i (k 8i..8i+3 of the thread's 32) and 2i+1
+                        // (k 8i+4..8i+7) of rows g, g+8; B the same k of the drafts' codes
 #pragma unroll
-                    for (int ww = 0; ww < WPW; ++ww) {
+                        for (int ww = 0; ww < WPW; ++ww)
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) {
+                                const uint32_t a0 = word_of<C::CPR>(b.c[ww][0], 2 * i);
+                                const uint32_t a1 = word_of<C::CPR>(b.c[ww][1], 2 * i);
+                                const uint32_t a2 = word_of<C::CPR>(b.c[ww][0], 2 * i + 1);
+                                const uint32_t a3 = word_of<C::CPR>(b.c[ww][1], 2 * i + 1);
+#pragma unroll
+                                for (int nt = 0; nt < NT; ++nt)
+                                    mma_e4m3(out[nt], a0, a1, a2, a3, hb[ww][nt][2 * i], hb[ww][nt][2 * i + 1]);
+                            }
+                    }
+#pragma unroll
+                    for (int ww = 0; ww < (C::W8A8 ? 0 : WPW); ++ww) {
                         uint32_t sg0 = 0u, sg1 = 0u, sh0 = 0u, sh1 = 0u;  // (s, s) f16x2 per row and block
                         if constexpr (C::NV) {
                             // blocks 2t, 2t+1 of the window: bytes 2t, 2t+1 of its 8 scale bytes
@@ -528,7 +661,7 @@ __global__ void __launch_bounds__(Cfg<FMT, K, MT>::THREADS, 1) gemv_mma_kernel(c
 #pragma unroll
                             for (int jj = 0; jj < 2; ++jj) {
                                 const int i = 2 * q4 + jj;
-                                uint32_t a0, a1, a2, a3;
+                                uint32_t a0 = 0u, a1 = 0u, a2 = 0u, a3 = 0u;
                                 if constexpr (C::NV) {
                                     a0 = fg[2 * jj];
                                     a1 = fh[2 * jj];
@@ -540,7 +673,7 @@ __global__ void __launch_bounds__(Cfg<FMT, K, MT>::THREADS, 1) gemv_mma_kernel(c
                                     a1 = e4m3x2_to_f16x2(wh & 0xFFFFu);
                                     a2 = e4m3x2_to_f16x2(wg >> 16);
                                     a3 = e4m3x2_to_f16x2(wh >> 16);
-                                } else {
+                                } else if constexpr (FMT == 3) {
                                     a0 = word_of<C::CPR>(b.c[ww][0], 2 * i);
                                     a1 = word_of<C::CPR>(b.c[ww][1], 2 * i);
                                     a2 = word_of<C::CPR>(b.c[ww][0], 2 * i + 1);
@@ -557,9 +690,19 @@ __global__ void __launch_bounds__(Cfg<FMT, K, MT>::THREADS, 1) gemv_mma_kernel(c
                         }
                     }
                 }
-                // loads of the tile P steps ahead go into the buffer just consumed
-                const int tn = ti + P;
-                if (tn < my_tiles) load_tile<FMT, K, MT>(buf[p], q, blockIdx.x + tn * gridDim.x, warp, g, t);
+                if constexpr (C::RING > 0) {
+                    // the stage just read takes the copies of the tile RING steps ahead
+                    __syncwarp();
+                    const int tn = ti + C::RING;
+                    if (tn < my_tiles)
+                        issue_stage<FMT, K, MT>(ring + (ti % C::RING) * C::RSTAGE, q, blockIdx.x + tn * gridDim.x, warp,
+                                                lane);
+                    cp_async_commit();
+                } else {
+                    // loads of the tile P steps ahead go into the buffer just consumed
+                    const int tn = ti + P;
+                    if (tn < my_tiles) load_tile<FMT, K, MT>(buf[p], q, blockIdx.x + tn * gridDim.x, warp, g, t);
+                }
                 // hand the partials to the reducer (wait for the slot to be free first)
                 if (ti >= RS && !*abort_flag && !mbar_wait(&empty_p[slot], ((ti / RS) - 1) & 1)) {
                     atomicOr(&a.ws->error, kDevErrTimeout);
@@ -589,6 +732,7 @@ __global__ void __launch_bounds__(Cfg<FMT, K, MT>::THREADS, 1) gemv_mma_kernel(c
             }
         }
     }
+    if constexpr (C::RING > 0) cp_async_wait_all();  // (only empty groups can be left)
     __syncthreads();
     if constexpr (!LOGITS) {
         if (tid < MT) {
@@ -610,7 +754,8 @@ inline cudaError_t launch_mma(const GemvArgs& a, cudaStream_t s) {
     auto kern = gemv_mma_kernel<FMT, K, MT, LOGITS>;
     const int sms = sm_count();
     if (sms <= 0) return cudaErrorInvalidDevice;
-    const size_t smem = C::LOADER ? static_cast<size_t>(C::SS) * C::SLOT : 0;
+    const size_t smem = C::LOADER ? static_cast<size_t>(C::SS) * C::SLOT
+                                  : static_cast<size_t>(C::RING) * C::RSTAGE * C::NW;
     static int occ[64] = {0};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);

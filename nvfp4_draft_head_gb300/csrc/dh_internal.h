@@ -50,6 +50,10 @@ cudaError_t launch_nvfp4_quantize(const uint16_t* W, int V, int K, const int32_t
 cudaError_t launch_fp8_quantize(const uint16_t* W, int V, int K, const int32_t* idx, int N,
                                 uint8_t* q, float* scale, Workspace* ws, cudaStream_t s);
 
+// Per-token dynamic E4M3 quantisation of BF16 rows h [M][K] (K % 16 == 0):
+// qx [M][K] codes, sx [M] scales. One CTA per row.
+cudaError_t launch_fp8_act_quantize(const uint16_t* h, int M, int K, uint8_t* qx, float* sx, cudaStream_t s);
+
 // Number of SMs of the current device (cached per device).
 int sm_count();
 

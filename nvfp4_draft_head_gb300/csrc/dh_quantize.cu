@@ -159,6 +159,48 @@ fp8_encode_kernel(const uint4* __restrict__ W, int V, int K, const int32_t* __re
     }
 }
 
+// Per-token dynamic E4M3 quantisation of the hidden states (the activation
+// half of the W8A8 head, "FP8 MTP draft stack for vLLM ...",
+// _Fp8DraftHeadMethod.apply): one CTA per row m; the row's max |h| by warp
+// shuffles and shared memory, then sx[m] = max(amax, 1e-12) / 448 and
+// qx[m, k] = E4M3_RNE(clamp(h[m, k] / sx[m], +-448)), eight codes per thread
+// and chunk. The draft-step kernel of the W8A8 head computes the same codes
+// with the same device functions.
+__global__ void __launch_bounds__(kQThreads)
+fp8_act_quantize_kernel(const uint4* __restrict__ h, int K, uint2* __restrict__ qx, float* __restrict__ sx) {
+    const int cpr = K / 8;  // 16-byte chunks of 8 BF16 per row
+    const uint4* row = h + static_cast<size_t>(blockIdx.x) * cpr;
+    float am = 0.0f;
+    for (int c = threadIdx.x; c < cpr; c += kQThreads) {
+        const uint4 v = row[c];
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) am = fmaxf(am, fmaxf(fabsf(bf16_lo(w[i])), fabsf(bf16_hi(w[i]))));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) am = fmaxf(am, __shfl_xor_sync(0xFFFFFFFFu, am, o));
+    __shared__ float s_red[kQThreads / 32];
+    if ((threadIdx.x & 31) == 0) s_red[threadIdx.x >> 5] = am;
+    __syncthreads();
+    float amax = s_red[0];
+#pragma unroll
+    for (int i = 1; i < kQThreads / 32; ++i) amax = fmaxf(amax, s_red[i]);
+    const float s = act_fp8_scale(amax);
+    if (threadIdx.x == 0) sx[blockIdx.x] = s;
+    uint2* out = qx + static_cast<size_t>(blockIdx.x) * cpr;
+    for (int c = threadIdx.x; c < cpr; c += kQThreads) {
+        const uint4 v = row[c];
+        out[c] = make_uint2(act_fp8_pair(v.x, s) | (act_fp8_pair(v.y, s) << 16),
+                            act_fp8_pair(v.z, s) | (act_fp8_pair(v.w, s) << 16));
+    }
+}
+
+cudaError_t launch_fp8_act_quantize(const uint16_t* h, int M, int K, uint8_t* qx, float* sx, cudaStream_t s) {
+    fp8_act_quantize_kernel<<<M, kQThreads, 0, s>>>(reinterpret_cast<const uint4*>(h), K,
+                                                     reinterpret_cast<uint2*>(qx), sx);
+    return cudaGetLastError();
+}
+
 static int quant_blocks(int N, int K) {
     const size_t chunks = static_cast<size_t>(N) * (K / 8);
     const size_t want = (chunks + kQThreads - 1) / kQThreads;

@@ -37,6 +37,26 @@ def test_every_declared_symbol_is_exported(L):
     assert set(names) == set(dh.EXPORTS)
 
 
+def test_library_has_no_process_wide_unique_symbols(L):
+    """Function-local statics of the launch templates (per-device caches) must
+    stay private to each loaded copy of the library (built with
+    -fno-gnu-unique), or a second copy would skip its own kernel set-up."""
+    import shutil
+    import subprocess
+    if shutil.which("nm") is None:
+        pytest.skip("nm not available")
+    out = subprocess.run(["nm", "-D", "--defined-only", dh.library_path()], capture_output=True, text=True).stdout
+    unique = [ln for ln in out.splitlines() if " u " in ln]
+    assert unique == [], unique[:3]
+
+
+def test_last_cuda_error_starts_clear(L):
+    name = C.c_char_p()
+    assert L.draft_head_last_cuda_error(C.byref(name)) == 0
+    assert name.value == b"cudaSuccess"
+    assert L.draft_head_last_cuda_error(None) == 0
+
+
 def test_status_strings_and_version(L):
     assert L.draft_head_abi_version() == 1
     for st in range(8):
@@ -137,6 +157,32 @@ def test_quantize_rejects_bad_arguments(L, args, status):
     st8 = L.fp8_quantize_rows(a["W"], a["V"], a["K"], a["idx"], a["N"], a["q"], a["g"], a["ws"],
                               a["ws_bytes"], None)
     assert st8 == status
+
+
+@pytest.mark.parametrize("args,status", [
+    (dict(h=None), dh.DH_ERR_ARG),
+    (dict(qx=None), dh.DH_ERR_ARG),
+    (dict(sx=None), dh.DH_ERR_ARG),
+    (dict(M=0), dh.DH_ERR_SHAPE),
+    (dict(K=24), dh.DH_ERR_SHAPE),     # K % 16 != 0
+    (dict(K=0), dh.DH_ERR_SHAPE),
+    (dict(h=0x10008), dh.DH_ERR_ALIGN),
+    (dict(qx=0x20004), dh.DH_ERR_ALIGN),
+    (dict(sx=0x30002), dh.DH_ERR_ALIGN),
+])
+def test_activation_quantize_rejects_bad_arguments(L, args, status):
+    a = dict(h=0x10000, M=4, K=2560, qx=0x20000, sx=0x30000)
+    a.update(args)
+    assert L.fp8_quantize_activations(a["h"], a["M"], a["K"], a["qx"], a["sx"], None) == status
+
+
+def test_w8a8_head_descriptor_checks(L):
+    d = _desc(fmt=dh.DH_FMT_FP8_W8A8, sf=None, scale=None)
+    assert L.draft_head_top_tokens(C.byref(d), H, 1, 0x300000, None, WS, 256, None) == dh.DH_ERR_ARG
+    d = _desc(fmt=dh.DH_FMT_FP8_W8A8, sf=None, K=300)
+    assert L.draft_head_top_tokens(C.byref(d), H, 1, 0x300000, None, WS, 256, None) == dh.DH_ERR_SHAPE
+    d = _desc(fmt=dh.DH_FMT_FP8_W8A8, sf=None)
+    assert L.draft_head_top_tokens(C.byref(d), H, 17, 0x300000, None, WS, 256, None) == dh.DH_ERR_SHAPE
 
 
 def test_binding_refuses_to_run_without_the_library(monkeypatch, tmp_path):

@@ -3,7 +3,8 @@
     M = 1 (fresh hidden states, the launch configuration the benchmark times);
   * the batch sweep M in {1, 2, 4, 8, 16} with planted near-ties (top-2 oracle
     gap < 1e-3 in 5 % of rows), both get_top_tokens and compute_logits;
-  * the 98,304-row FP8 head: quantise bit-exact, M = 1 and 4, both paths;
+  * the 98,304-row FP8 head: quantise bit-exact, M = 1 and 4, both paths,
+    W8A16 and W8A8 (per-token FP8 hidden states);
   * the full-vocabulary BF16 head (the stock drafter read) at M = 1.
 The oracle computes every output here (its fp64 GEMV over a whole head takes
 about a second per draft row on one core)."""
@@ -15,7 +16,7 @@ import nvfp4_draft_head_gb300 as dh
 import oracle
 import synthetic as syn
 from parity_util import Workload, check_argmax_rows, check_logits, ids_to_rows, plant_near_ties
-from test_parity_gpu import dev, dev_bf16, pack_reference, run_step
+from test_parity_gpu import dev, dev_bf16, pack_reference, run_step, run_step_w8a8
 
 pytestmark = pytest.mark.gpu
 
@@ -109,6 +110,11 @@ def test_fp8_98k_head(W_full, W_dev):
     for M in (1, 4):
         h = syn.hidden_bf16(syn.hidden_seed(2, M), M, wl.K)
         run_step(head, h, oracle.FMT_FP8, q_o, None, s_o, wl.idx, wl.n_kept, wl.V, f"fp8 98k M={M}")
+    # the same head run W8A8: hidden states quantised per token inside the step
+    w8a8 = dh.DraftHead(dh.DH_FMT_FP8_W8A8, wl.V, q, idx, wl.n_kept, scale=s, idx_ascending=True)
+    for M in (1, 4):
+        h = syn.hidden_bf16(syn.hidden_seed(2, 10 + M), M, wl.K)
+        run_step_w8a8(w8a8, h, q_o, s_o, wl.idx, wl.n_kept, wl.V, f"fp8 w8a8 98k M={M}")
 
 
 def test_bf16_full_vocabulary_head(W_full, W_dev):

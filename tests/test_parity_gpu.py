@@ -70,13 +70,26 @@ def gpu_fp8(wl, ascending=True):
 
 def run_step(head, h_bits, fmt, q_or, sf_or, s_or, idx, n_kept, V, what):
     """top_tokens + compute_logits for one batch of hidden rows, both checked."""
+    y, A = oracle.gemv(fmt, q_or, sf_or, s_or, h_bits)
+    return check_step(head, h_bits, y, A, idx, n_kept, V, what)
+
+
+def run_step_w8a8(head, h_bits, q_or, s_or, idx, n_kept, V, what):
+    """The same for the W8A8 FP8 head: the oracle quantises h per token itself."""
+    qx, sx = oracle.fp8_act_quantize(h_bits)
+    y, A = oracle.gemv_w8a8(q_or, s_or, qx, sx)
+    return check_step(head, h_bits, y, A, idx, n_kept, V, what)
+
+
+def check_step(head, h_bits, y, A, idx, n_kept, V, what):
+    """Run top_tokens + compute_logits on the GPU and check them against the
+    oracle's logits y (and tolerance scales A) of every head row."""
     h = dev_bf16(h_bits)
     M = h_bits.shape[0]
     top = torch.empty(M, dtype=torch.float32, device="cuda")
     ids = head.top_tokens(h, top=top).cpu().numpy()
     out = head.compute_logits(h).cpu().numpy()
     assert head.device_error() == 0
-    y, A = oracle.gemv(fmt, q_or, sf_or, s_or, h_bits)
     rows = ids_to_rows(ids, idx, n_kept) if idx is not None else ids
     exact = check_argmax_rows(rows, y, A, n_kept, what)
     check_logits(top.cpu().numpy()[:, None], y[np.arange(M), rows][:, None],
@@ -133,6 +146,66 @@ def test_tiny_fp8_step(tiny, M, ascending):
     h = syn.hidden_bf16(syn.hidden_seed(0, 500 + M), M, tiny.K)
     run_step(head, h, oracle.FMT_FP8, q_o, None, s_o, tiny.idx, tiny.n_kept, tiny.V,
              f"tiny fp8 M={M} ascending={ascending}")
+
+
+def special_act_rows(K):
+    """Hidden rows that exercise the per-token quantiser's edges: all zeros (the
+    1e-12 clamp), one huge value among small ones (codes flushed towards zero,
+    subnormal E4M3 codes), every value equal (all codes 448), values at BF16's
+    range ends, alternating signs."""
+    rows = np.zeros((6, K), np.uint16)
+    r1 = syn.hidden_bf16(21, 1, K)[0].copy()
+    r1[7] = syn.f32_to_bf16_bits(np.float32([3.0e5]))[0]
+    rows[1] = r1
+    rows[2] = syn.f32_to_bf16_bits(np.full(K, -0.8125, np.float32))
+    big = np.where(np.arange(K) % 3 == 0, 1.0e30, -2.5e-30).astype(np.float32)
+    rows[3] = syn.f32_to_bf16_bits(big)
+    rows[4] = syn.f32_to_bf16_bits(np.where(np.arange(K) % 2 == 0, 1.0, -1.0).astype(np.float32))
+    rows[5] = syn.hidden_bf16(22, 1, K)[0]
+    return rows
+
+
+def test_tiny_fp8_act_quantize_bit_exact(tiny):
+    for M, seed in ((1, 31), (5, 32), (16, 33), (37, 34)):
+        h = syn.hidden_bf16(seed, M, tiny.K)
+        qx, sx = dh.fp8_quantize_activations(dev_bf16(h))
+        qx_o, sx_o = oracle.fp8_act_quantize(h)
+        assert np.array_equal(qx.cpu().numpy(), qx_o), f"codes M={M}"
+        assert np.array_equal(sx.cpu().numpy().view(np.uint32), sx_o.view(np.uint32)), f"scales M={M}"
+    for K in (tiny.K, 2560, 16, 4112):
+        h = special_act_rows(K)
+        qx, sx = dh.fp8_quantize_activations(dev_bf16(h))
+        qx_o, sx_o = oracle.fp8_act_quantize(h)
+        assert np.array_equal(qx.cpu().numpy(), qx_o), f"special rows K={K}"
+        assert np.array_equal(sx.cpu().numpy().view(np.uint32), sx_o.view(np.uint32))
+
+
+@pytest.mark.parametrize("M", [1, 2, 4, 7, 16])
+def test_tiny_w8a8_step(tiny, M):
+    _, (q, s) = gpu_fp8(tiny)
+    head = dh.DraftHead(dh.DH_FMT_FP8_W8A8, tiny.V, q, dev(tiny.idx), tiny.n_kept, scale=s, idx_ascending=M != 7)
+    q_o, s_o = tiny.fp8()
+    for step in range(2):
+        h = syn.hidden_bf16(syn.hidden_seed(0, 600 + 10 * M + step), M, tiny.K)
+        run_step_w8a8(head, h, q_o, s_o, tiny.idx, tiny.n_kept, tiny.V, f"tiny w8a8 M={M} step={step}")
+
+
+def test_w8a8_special_rows_and_sizes(tiny):
+    """Quantiser edge rows through the fused W8A8 step, and the other hidden
+    sizes (K = 2560: 20 windows over 20 warps; K = 5120: two windows per warp)."""
+    _, (q, s) = gpu_fp8(tiny)
+    head = dh.DraftHead(dh.DH_FMT_FP8_W8A8, tiny.V, q, dev(tiny.idx), tiny.n_kept, scale=s, idx_ascending=True)
+    q_o, s_o = tiny.fp8()
+    run_step_w8a8(head, special_act_rows(tiny.K), q_o, s_o, tiny.idx, tiny.n_kept, tiny.V, "w8a8 special rows")
+    for V, K, n_kept in ((3000, 5120, 700), (2000, 2560, 129)):
+        wl = Workload(177 + K, V, K, n_kept, 5, 188 + n_kept)
+        _, (q2, s2) = gpu_fp8(wl)
+        q2_o, s2_o = wl.fp8()
+        head2 = dh.DraftHead(dh.DH_FMT_FP8_W8A8, V, q2, dev(wl.idx), wl.n_kept, scale=s2, idx_ascending=True)
+        for M in (1, 9):
+            run_step_w8a8(head2, syn.hidden_bf16(990 + M + K, M, K), q2_o, s2_o, wl.idx, wl.n_kept, V,
+                          f"w8a8 V={V} K={K} M={M}")
+        run_step_w8a8(head2, special_act_rows(K), q2_o, s2_o, wl.idx, wl.n_kept, V, f"w8a8 special K={K}")
 
 
 @pytest.mark.parametrize("M", [1, 2, 16])
