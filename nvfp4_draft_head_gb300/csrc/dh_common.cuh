@@ -208,16 +208,6 @@ __device__ __forceinline__ void cp_async_wait_all() {
     asm volatile("cp.async.wait_all;" ::: "memory");
 }
 
-__device__ __forceinline__ void cp_async_commit() {
-    asm volatile("cp.async.commit_group;" ::: "memory");
-}
-
-// Wait until at most N of this thread's committed cp.async groups are pending.
-template <int N>
-__device__ __forceinline__ void cp_async_wait_group() {
-    asm volatile("cp.async.wait_group %0;" :: "n"(N) : "memory");
-}
-
 // L2 policy for data read once per step (the head): evict first.
 __device__ __forceinline__ uint64_t policy_evict_first() {
     uint64_t p;

@@ -54,8 +54,8 @@
 namespace dh {
 namespace mma {
 
-#ifndef DH_RING_STAGES
-#define DH_RING_STAGES 0  // packed NVFP4: cp.async shared-memory stages per compute warp (0: register loads)
+#ifndef DH_NW_MAX
+#define DH_NW_MAX 20  // compute warps per CTA at most (fewer: several windows per warp, 2 CTAs per SM)
 #endif
 
 constexpr int cmin(int a, int b) { return a < b ? a : b; }
@@ -69,7 +69,7 @@ constexpr int kIdCap = 48;
 template <int FMT, int K, int MT>
 struct Cfg {
     static constexpr int NWIN = K / 128;                     // 128-wide k-windows per row
-    static constexpr int NW = NWIN <= 20 ? NWIN : 20;        // warps per CTA
+    static constexpr int NW = NWIN <= DH_NW_MAX ? NWIN : DH_NW_MAX;  // compute warps per CTA
     static constexpr int WPW = NWIN / NW;                    // windows per warp
     static constexpr int NT = MT <= 8 ? 1 : 2;               // n8 tiles of drafts
     static constexpr bool NV = (FMT == 1 || FMT == 4);       // NVFP4 (canonical or packed layout)
@@ -86,16 +86,7 @@ struct Cfg {
     // register loads in flight (tiles ahead) when the code bytes come straight to
     // registers; two at 16 drafts, where the h fragments of two n8 tiles leave no
     // room for a third within the 80 registers 21+ warps per SM allow
-    // Packed NVFP4 with a shared-memory ring: each compute warp keeps RING tiles
-    // of its windows in flight as 16-byte cp.async copies (no registers held),
-    // within ~184 KB of shared memory (~140 KB at 16 drafts, whose partial-sum
-    // ring is larger).
-    static constexpr int RSTAGE = WPW * (16 * 64 + 16 * 8);  // bytes of one warp's stage
-    static constexpr int RING =
-        (PACKED && DH_RING_STAGES > 0)
-            ? cmax(2, cmin(DH_RING_STAGES, (MT >= 16 ? 140 * 1024 : 184 * 1024) / (NW * RSTAGE)))
-            : 0;
-    static constexpr int P = RING > 0 ? 1 : cmax(1, cmin(MT >= 16 ? 2 : 3, 48 / TILE_REGS));
+    static constexpr int P = cmax(1, cmin(MT >= 16 ? 2 : 3, 48 / TILE_REGS));
     // Canonical NVFP4 layout: a loader warp streams each tile's scale bytes
     // into a shared-memory ring with 1-D bulk copies.
     static constexpr bool SCALES = (FMT == 1);
@@ -183,33 +174,6 @@ __device__ __forceinline__ void load_tile(TileBuf<FMT, K, MT>& b, const uint8_t*
     }
 }
 
-// Ring mode: one warp copies its windows' blocks of a tile into a stage.
-template <int FMT, int K, int MT>
-__device__ __forceinline__ void issue_stage(uint8_t* stage, const uint8_t* q, int tile, int warp, int lane) {
-    using C = Cfg<FMT, K, MT>;
-#pragma unroll
-    for (int ww = 0; ww < C::WPW; ++ww) {
-        const uint8_t* src = q + (static_cast<size_t>(tile) * C::NWIN + warp + ww * C::NW) * C::WBLK;
-        uint8_t* dst = stage + ww * C::WBLK;
-        for (int c = lane; c < C::WBLK / 16; c += 32) cp_async16(dst + 16 * c, src + 16 * c);
-    }
-}
-
-// Ring mode: this thread's fragments of a staged tile (same layout as load_tile's).
-template <int FMT, int K, int MT>
-__device__ __forceinline__ void fetch_stage(TileBuf<FMT, K, MT>& b, const uint8_t* stage, int g, int t) {
-    using C = Cfg<FMT, K, MT>;
-#pragma unroll
-    for (int ww = 0; ww < C::WPW; ++ww) {
-        const uint8_t* st = stage + ww * C::WBLK;
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            b.c[ww][h][0] = *reinterpret_cast<const uint4*>(st + (g + 8 * h) * 64 + 16 * t);
-            b.s[ww][h] = *reinterpret_cast<const uint2*>(st + 16 * 64 + (g + 8 * h) * 8);
-        }
-    }
-}
-
 // Byte i (0..15) of a 16-byte piece.
 __device__ __forceinline__ uint32_t byte_of(const uint4& v, int i) {
     const uint32_t w = i < 4 ? v.x : (i < 8 ? v.y : (i < 12 ? v.z : v.w));
@@ -231,7 +195,8 @@ __device__ __forceinline__ uint32_t word_of(const uint4 (&v)[CPR], int i) {
 }
 
 template <int FMT, int K, int MT, bool LOGITS>
-__global__ void __launch_bounds__(Cfg<FMT, K, MT>::THREADS, 1) gemv_mma_kernel(const GemvArgs a) {
+__global__ void __launch_bounds__(Cfg<FMT, K, MT>::THREADS, Cfg<FMT, K, MT>::NW <= 10 ? 2 : 1)
+    gemv_mma_kernel(const GemvArgs a) {
     using C = Cfg<FMT, K, MT>;
     constexpr int NW = C::NW, WPW = C::WPW, NT = C::NT, P = C::P, KW = K / 2, RS = C::RS;
     constexpr int NRED = 16 * MT;  // (row, draft) results of a tile
@@ -257,22 +222,12 @@ __global__ void __launch_bounds__(Cfg<FMT, K, MT>::THREADS, 1) gemv_mma_kernel(c
     const uint8_t* q = static_cast<const uint8_t*>(a.q);
     volatile int* abort_flag = &s_abort;
 
-    // Issue the first P tiles' loads (ring mode: the first RING tiles' copies)
-    // before anything else (compute warps).
+    // Issue the first P tiles' loads before anything else (compute warps).
     TileBuf<FMT, K, MT> buf[P];
-    uint8_t* ring = s_scales + ((C::RING > 0 && warp < NW) ? warp * C::RING * C::RSTAGE : 0);  // this warp's stages
     if (warp < NW) {
-        if constexpr (C::RING > 0) {
-#pragma unroll 1
-            for (int i = 0; i < C::RING; ++i) {
-                if (i < my_tiles) issue_stage<FMT, K, MT>(ring + i * C::RSTAGE, q, blockIdx.x + i * gridDim.x, warp, lane);
-                cp_async_commit();
-            }
-        } else {
 #pragma unroll
-            for (int p = 0; p < P; ++p)
-                if (p < my_tiles) load_tile<FMT, K, MT>(buf[p], q, blockIdx.x + p * gridDim.x, warp, g, t);
-        }
+        for (int p = 0; p < P; ++p)
+            if (p < my_tiles) load_tile<FMT, K, MT>(buf[p], q, blockIdx.x + p * gridDim.x, warp, g, t);
     }
 
     if (tid == 0) {
@@ -459,20 +414,39 @@ __global__ void __launch_bounds__(Cfg<FMT, K, MT>::THREADS, 1) gemv_mma_kernel(c
                 if (t == 0) s_amx[warp][d] = am;
             }
             named_bar_sync(2, NW * 32);  // compute warps only
+            float sx_own[NT];  // scale of this lane's draft g + 8 nt
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
                 const int d = g + 8 * nt;
                 float am = 0.0f;
                 for (int w2 = 0; w2 < NW; ++w2) am = fmaxf(am, s_amx[w2][d]);
-                const float sx = act_fp8_scale(am);
+                sx_own[nt] = act_fp8_scale(am);
+                unscale[nt][0] = __shfl_sync(0xFFFFFFFFu, sx_own[nt], 4 * (2 * t));
+                unscale[nt][1] = __shfl_sync(0xFFFFFFFFu, sx_own[nt], 4 * (2 * t + 1));
 #pragma unroll
                 for (int ww = 0; ww < WPW; ++ww)
 #pragma unroll
-                    for (int j = 0; j < 8; ++j)
-                        hb[ww][nt][j] = act_fp8_pair(hb[ww][nt][2 * j], sx) |
-                                        (act_fp8_pair(hb[ww][nt][2 * j + 1], sx) << 16);
-                unscale[nt][0] = __shfl_sync(0xFFFFFFFFu, sx, 4 * (2 * t));
-                unscale[nt][1] = __shfl_sync(0xFFFFFFFFu, sx, 4 * (2 * t + 1));
+                    for (int j = 0; j < 8; ++j) hb[ww][nt][j] = 0u;
+            }
+            // The warp encodes each live draft together: lane l takes the 4 codes
+            // of k = 128 w + 4 l .. 4 l + 3 (4 IEEE divisions instead of 32 per
+            // lane and draft), then lane (g, t) collects words 8 t .. 8 t + 7 of
+            // its own draft g + 8 nt.
+#pragma unroll
+            for (int d = 0; d < MT; ++d) {
+                if (d >= a.M) break;
+                const float sx = __shfl_sync(0xFFFFFFFFu, sx_own[d / 8], 4 * (d % 8));
+#pragma unroll
+                for (int ww = 0; ww < WPW; ++ww) {
+                    const int kw = (128 * (warp + ww * NW) + 4 * lane) / 2;  // u32 index of the lane's 4 values
+                    const uint32_t w0 = __ldg(h32 + d * KW + kw), w1 = __ldg(h32 + d * KW + kw + 1);
+                    const uint32_t word = act_fp8_pair(w0, sx) | (act_fp8_pair(w1, sx) << 16);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const uint32_t v = __shfl_sync(0xFFFFFFFFu, word, 8 * t + j);
+                        if (g == d % 8) hb[ww][d / 8][j] = v;
+                    }
+                }
             }
         }
 #pragma unroll
@@ -540,13 +514,7 @@ __global__ void __launch_bounds__(Cfg<FMT, K, MT>::THREADS, 1) gemv_mma_kernel(c
                 if (ti >= my_tiles) break;
                 TileBuf<FMT, K, MT>& b = buf[p];
                 const int slot = ti % RS;
-                if constexpr (C::RING > 0) {
-                    // tile ti's copies are the oldest group but RING - 1; every lane's
-                    // copies have landed once all lanes passed the wait
-                    cp_async_wait_group<C::RING - 1>();
-                    __syncwarp();
-                    fetch_stage<FMT, K, MT>(b, ring + (ti % C::RING) * C::RSTAGE, g, t);
-                }
+
                 if constexpr (C::SCALES) {
                     const int ss = ti % C::SS;
                     if (!*abort_flag && !mbar_wait(&full_s[ss], (ti / C::SS) & 1)) {
@@ -586,6 +554,7 @@ __global__ void __launch_bounds__(Cfg<FMT, K, MT>::THREADS, 1) gemv_mma_kernel(c
                                 mma_f16(d, fg0[j], fh0[j], fg1[j], fh1[j], hb[ww][0][i], hb[ww][0][8 + i]);
                             }
                         }
+
                         // scales of blocks blk0, blk1 of rows g, g+8 (bytes of the window's 8)
                         const uint32_t sel = static_cast<uint32_t>(blk0) | (static_cast<uint32_t>(blk1) << 4);
                         uint32_t s01g, s01h;
@@ -690,19 +659,9 @@ __global__ void __launch_bounds__(Cfg<FMT, K, MT>::THREADS, 1) gemv_mma_kernel(c
                         }
                     }
                 }
-                if constexpr (C::RING > 0) {
-                    // the stage just read takes the copies of the tile RING steps ahead
-                    __syncwarp();
-                    const int tn = ti + C::RING;
-                    if (tn < my_tiles)
-                        issue_stage<FMT, K, MT>(ring + (ti % C::RING) * C::RSTAGE, q, blockIdx.x + tn * gridDim.x, warp,
-                                                lane);
-                    cp_async_commit();
-                } else {
-                    // loads of the tile P steps ahead go into the buffer just consumed
-                    const int tn = ti + P;
-                    if (tn < my_tiles) load_tile<FMT, K, MT>(buf[p], q, blockIdx.x + tn * gridDim.x, warp, g, t);
-                }
+                // loads of the tile P steps ahead go into the buffer just consumed
+                const int tn = ti + P;
+                if (tn < my_tiles) load_tile<FMT, K, MT>(buf[p], q, blockIdx.x + tn * gridDim.x, warp, g, t);
                 // hand the partials to the reducer (wait for the slot to be free first)
                 if (ti >= RS && !*abort_flag && !mbar_wait(&empty_p[slot], ((ti / RS) - 1) & 1)) {
                     atomicOr(&a.ws->error, kDevErrTimeout);
@@ -732,7 +691,6 @@ __global__ void __launch_bounds__(Cfg<FMT, K, MT>::THREADS, 1) gemv_mma_kernel(c
             }
         }
     }
-    if constexpr (C::RING > 0) cp_async_wait_all();  // (only empty groups can be left)
     __syncthreads();
     if constexpr (!LOGITS) {
         if (tid < MT) {
@@ -754,8 +712,7 @@ inline cudaError_t launch_mma(const GemvArgs& a, cudaStream_t s) {
     auto kern = gemv_mma_kernel<FMT, K, MT, LOGITS>;
     const int sms = sm_count();
     if (sms <= 0) return cudaErrorInvalidDevice;
-    const size_t smem = C::LOADER ? static_cast<size_t>(C::SS) * C::SLOT
-                                  : static_cast<size_t>(C::RING) * C::RSTAGE * C::NW;
+    const size_t smem = C::LOADER ? static_cast<size_t>(C::SS) * C::SLOT : 0;
     static int occ[64] = {0};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
