@@ -478,6 +478,13 @@ def run_suite(args):
     ids = torch.empty(1, dtype=torch.int32, device=dev)
     calls = [(lambda i=i: hf.top_tokens(hs[i % 64: i % 64 + 1], ids=ids)) for i in range(min(steps, 200))]
     line("bf16 248,320 x 2560 top_tokens M=1", graph_us(calls), 248_320 * K_HID * 2 + 2 * K_HID + 4)
+    # truncated 40,960-row BF16 draft head read in place (six copies = 1.26 GB > L2)
+    tr = [dh.bf16_truncated_head(Wd[i * 40_960:], 40_960) for i in range(6)]
+    for M in (1, 4):
+        ids = torch.empty(M, dtype=torch.int32, device=dev)
+        calls = [(lambda i=i: tr[i % 6].top_tokens(hsM[i % 8, :M], ids=ids)) for i in range(steps)]
+        line(f"bf16 truncated 40,960 x 2560 top_tokens M={M}", graph_us(calls), 40_960 * K_HID * 2 + M * (2 * K_HID + 4),
+             {"M": M})
 
     # tiny head (L2-resident, latency-bound)
     ct = syn.TINY

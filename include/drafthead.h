@@ -207,6 +207,22 @@ int draft_head_top_tokens(const dh_head_t *hd, const void *h, int M, int32_t *id
 int draft_head_compute_logits(const dh_head_t *hd, const void *h, int M, float *out,
                               void *ws, size_t ws_bytes, void *stream);
 
+/* NVFP4 W4A16 linear layer of the MTP block ("q38_draft.py", MTP_QUANT_KEYS:
+ * fc_embedding, fc_hidden, qkv_proj, o_proj, shared_expert are quantised with
+ * the same NVFP4 recipe as the head): for m < M and n < N,
+ *   y[m, n] = g * sum_k w'[n, k] * x[m, k]   (fp32 accumulation).
+ *   w   an NVFP4 weight in the packed layout: fmt = DH_FMT_NVFP4_PACKED, N
+ *       output features (N % 64 == 0), K input features, q = the bytes from
+ *       nvfp4_pack_head, scale = &g; V, n_kept, sf, idx and flags are ignored.
+ *       Quantise the [N][K] BF16 weight with nvfp4_quantize_rows (idx = 0..N-1).
+ *       K in {256, 512, 1024, 2048, 2560, 4096, 5120}.
+ *   x   BF16 [M][K] row-major, 16-byte aligned; 1 <= M <= 16.
+ *   y   fp32 [M][N] row-major, 16-byte aligned; every entry is written.
+ *   ws  a draft-step workspace (draft_head_workspace_bytes bytes, initialised).
+ * One kernel launch; capturable in a CUDA graph. */
+int nvfp4_linear(const dh_head_t *w, const void *x, int M, float *y, void *ws, size_t ws_bytes,
+                 void *stream);
+
 /* get_top_tokens without a caller workspace, for callers that cannot
  * allocate device memory: a plugin hook that is handed only its input and
  * output buffers, or a serving loop that forbids cudaMalloc because it can

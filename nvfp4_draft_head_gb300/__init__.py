@@ -11,6 +11,7 @@ Names follow the C ABI in include/drafthead.h:
   fp8_quantize_activations per-token FP8 E4M3 codes of hidden states (W8A8)
   DraftHead.top_tokens     get_top_tokens: dh_idx[argmax_n (W_q h)]
   DraftHead.compute_logits compute_logits: -inf row + logits at dh_idx
+  NVFP4Linear              nvfp4_linear: an MTP-block linear, y = x W'^T
 """
 from __future__ import annotations
 
@@ -35,7 +36,7 @@ EXPORTS = (
     "fp8_quantize_rows", "draft_head_workspace_bytes", "draft_head_workspace_init",
     "draft_head_top_tokens", "draft_head_compute_logits", "draft_head_read_device_error",
     "draft_head_status_string", "draft_head_abi_version", "draft_head_top_tokens_static",
-    "nvfp4_pack_head", "fp8_quantize_activations", "draft_head_last_cuda_error",
+    "nvfp4_pack_head", "fp8_quantize_activations", "draft_head_last_cuda_error", "nvfp4_linear",
 )
 
 _lib = None
@@ -91,6 +92,7 @@ def lib():
         L.nvfp4_pack_head.argtypes = [P, P, I, I, P, P]
         L.fp8_quantize_activations.argtypes = [P, I, I, P, P, P]
         L.draft_head_last_cuda_error.argtypes = [C.POINTER(C.c_char_p)]
+        L.nvfp4_linear.argtypes = [C.POINTER(dh_head_t), P, I, P, P, S, P]
         _lib = L
     return _lib
 
@@ -301,6 +303,57 @@ def fp8_head(W: torch.Tensor, keep, w8a8: bool = False, stream=None) -> DraftHea
                      idx_ascending=True)
 
 
+class NVFP4Linear:
+    """An NVFP4 W4A16 linear layer (an MTP-block linear): weight W [N, K] BF16
+    quantised with the head's recipe and repacked tile-major; forward(x) =
+    x W'^T in fp32. N % 64 == 0."""
+
+    def __init__(self, W: torch.Tensor, stream=None):
+        N, K = W.shape
+        idx = torch.arange(N, dtype=torch.int32, device=W.device)
+        q, sf, g = nvfp4_quantize_rows(W, idx, stream)
+        self.q, self.sf, self.g = q, sf, g
+        self.packed = nvfp4_pack_head(q, sf, stream)
+        self.N, self.K = N, K
+        self.desc = dh_head_t(DH_FMT_NVFP4_PACKED, N, K, N, N, _ptr(self.packed), None, _ptr(g), None, 0)
+        self.ws_bytes = lib().draft_head_workspace_bytes(C.byref(self.desc), DH_MAX_M)
+        self.ws = _workspace(self.ws_bytes, W.device)
+
+    def with_storage(self, packed: torch.Tensor) -> "NVFP4Linear":
+        """The same layer read from another copy of its packed bytes."""
+        other = object.__new__(NVFP4Linear)
+        other.__dict__.update(self.__dict__)
+        other.packed = packed
+        other.desc = dh_head_t(DH_FMT_NVFP4_PACKED, self.N, self.K, self.N, self.N, _ptr(packed), None,
+                               _ptr(self.g), None, 0)
+        return other
+
+    def forward(self, x: torch.Tensor, y: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+        if x.dtype != torch.bfloat16 or x.dim() != 2 or x.shape[1] != self.K or not x.is_contiguous():
+            raise ValueError(f"x must be a contiguous [M, {self.K}] bfloat16 tensor")
+        M = x.shape[0]
+        if y is None:
+            y = torch.empty((M, self.N), dtype=torch.float32, device=x.device)
+        _check("nvfp4_linear",
+               lib().nvfp4_linear(C.byref(self.desc), x.data_ptr(), M, y.data_ptr(), self.ws.data_ptr(),
+                                  self.ws_bytes, _stream(stream)))
+        return y
+
+    __call__ = forward
+
+    def device_error(self, stream=None) -> int:
+        return draft_head_read_device_error(self.ws, stream)
+
+
 def bf16_full_head(W: torch.Tensor) -> DraftHead:
     """The stock full-vocabulary BF16 head (the row is the id)."""
     return DraftHead(DH_FMT_BF16, W.shape[0], W, None, W.shape[0])
+
+
+def bf16_truncated_head(W: torch.Tensor, n_rows: int) -> DraftHead:
+    """A truncated BF16 draft head: the first n_rows rows of the target head
+    (ids 0 .. n_rows-1, n_rows % 64 == 0), read in place; compute_logits still
+    writes full-vocabulary rows (-inf past n_rows)."""
+    if n_rows % 64 or not 0 < n_rows <= W.shape[0]:
+        raise ValueError("n_rows must be a multiple of 64 within the head")
+    return DraftHead(DH_FMT_BF16, W.shape[0], W[:n_rows], None, n_rows)

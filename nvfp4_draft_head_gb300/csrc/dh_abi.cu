@@ -212,6 +212,33 @@ int draft_head_compute_logits(const dh_head_t* hd, const void* h, int M, float* 
     return cuda_status(dh::launch_gemv(a, s));
 }
 
+int nvfp4_linear(const dh_head_t* w, const void* x, int M, float* y, void* ws, size_t ws_bytes, void* stream) {
+    if (w == nullptr || w->q == nullptr || w->scale == nullptr || x == nullptr || y == nullptr) return DH_ERR_ARG;
+    if (w->fmt != DH_FMT_NVFP4_PACKED) return DH_ERR_ARG;
+    if (w->N <= 0 || w->N % 64 != 0 || !dh::linear_supported(w->K)) return DH_ERR_SHAPE;
+    if (M < 1 || M > DH_MAX_M) return DH_ERR_SHAPE;
+    if (static_cast<long long>(M) * w->N >= (1ll << 31)) return DH_ERR_SHAPE;
+    if (!aligned(w->q, 16) || !aligned(w->scale, 4) || !aligned(x, 16) || !aligned(y, 16)) return DH_ERR_ALIGN;
+    int st = check_ws(ws, ws_bytes, sizeof(dh::Workspace));
+    if (st != DH_OK) return st;
+    dh::GemvArgs a;
+    std::memset(&a, 0, sizeof a);
+    a.fmt = w->fmt;
+    a.K = w->K;
+    a.V = w->N;       // row n of the weight writes column n of y
+    a.N = w->N;
+    a.n_kept = w->N;
+    a.q = w->q;
+    a.scale = w->scale;
+    a.idx = nullptr;
+    a.idx_ascending = 1;
+    a.h = static_cast<const uint16_t*>(x);
+    a.M = M;
+    a.out = y;
+    a.ws = static_cast<dh::Workspace*>(ws);
+    return cuda_status(dh::launch_gemv(a, static_cast<cudaStream_t>(stream)));
+}
+
 int draft_head_read_device_error(void* ws, int* err, void* stream) {
     if (ws == nullptr || err == nullptr) return DH_ERR_ARG;
     if (!aligned(ws, DH_WORKSPACE_ALIGN)) return DH_ERR_WORKSPACE;

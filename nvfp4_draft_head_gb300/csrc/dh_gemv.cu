@@ -11,6 +11,8 @@ cudaError_t launch_gemv_fp8(const GemvArgs& a, cudaStream_t s);
 cudaError_t launch_gemv_bf16(const GemvArgs& a, cudaStream_t s);
 cudaError_t launch_gemv_nvfp4_packed(const GemvArgs& a, cudaStream_t s);
 cudaError_t launch_gemv_fp8_w8a8(const GemvArgs& a, cudaStream_t s);
+bool linear_extra_k(int K);
+cudaError_t launch_linear_nvfp4_packed_extra(const GemvArgs& a, cudaStream_t s);
 
 __global__ void fill_neg_inf_kernel(float4* out4, size_t n4, float* tail, int ntail) {
     const float ninf = __uint_as_float(0xFF800000u);
@@ -43,7 +45,10 @@ bool gemv_supported(int fmt, int K) {
     return false;
 }
 
+bool linear_supported(int K) { return gemv_supported(4, K) || linear_extra_k(K); }
+
 cudaError_t launch_gemv(const GemvArgs& a, cudaStream_t s) {
+    if (a.fmt == 4 && a.out != nullptr && linear_extra_k(a.K)) return launch_linear_nvfp4_packed_extra(a, s);
     if (!gemv_supported(a.fmt, a.K)) return cudaErrorInvalidValue;
     if (a.fmt == 1) return launch_gemv_nvfp4(a, s);
     if (a.fmt == 2) return launch_gemv_fp8(a, s);

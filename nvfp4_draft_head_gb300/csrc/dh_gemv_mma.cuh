@@ -54,11 +54,21 @@
 namespace dh {
 namespace mma {
 
+#ifndef DH_P_BUDGET
+#define DH_P_BUDGET 64  // registers per thread for tile loads in flight plus the h fragments
+#endif
 #ifndef DH_NW_MAX
 #define DH_NW_MAX 20  // compute warps per CTA at most (fewer: several windows per warp, 2 CTAs per SM)
 #endif
 
 constexpr int cmin(int a, int b) { return a < b ? a : b; }
+
+// Largest divisor of n that is at most cap.
+constexpr int largest_divisor_at_most(int n, int cap) {
+    for (int d = cap < n ? cap : n; d > 1; --d)
+        if (n % d == 0) return d;
+    return 1;
+}
 constexpr int cmax(int a, int b) { return a > b ? a : b; }
 
 // Tiles per CTA whose dh_idx entries the reducer stages in shared memory
@@ -69,7 +79,7 @@ constexpr int kIdCap = 48;
 template <int FMT, int K, int MT>
 struct Cfg {
     static constexpr int NWIN = K / 128;                     // 128-wide k-windows per row
-    static constexpr int NW = NWIN <= DH_NW_MAX ? NWIN : DH_NW_MAX;  // compute warps per CTA
+    static constexpr int NW = largest_divisor_at_most(NWIN, DH_NW_MAX);  // compute warps per CTA
     static constexpr int WPW = NWIN / NW;                    // windows per warp
     static constexpr int NT = MT <= 8 ? 1 : 2;               // n8 tiles of drafts
     static constexpr bool NV = (FMT == 1 || FMT == 4);       // NVFP4 (canonical or packed layout)
@@ -83,10 +93,11 @@ struct Cfg {
     static constexpr int SFB = NV ? K / 16 : 0;               // scale bytes per head row
     static constexpr int WBLK = 16 * WB + 16 * 8;             // packed: bytes of one (tile, window) block
     static constexpr int TILE_REGS = WPW * (8 * CPR + (NV ? 4 : 0));
-    // register loads in flight (tiles ahead) when the code bytes come straight to
-    // registers; two at 16 drafts, where the h fragments of two n8 tiles leave no
-    // room for a third within the 80 registers 21+ warps per SM allow
-    static constexpr int P = cmax(1, cmin(MT >= 16 ? 2 : 3, 48 / TILE_REGS));
+    // tiles of loads in flight in registers: as many as fit, next to the h
+    // fragments (16 registers per window and n8 tile), in the 80 registers that
+    // 21+ warps per SM allow: three with one window per warp and one n8 tile,
+    // two at 16 drafts, one with two windows per warp (K = 4096, 5120)
+    static constexpr int P = cmax(1, cmin(MT >= 16 ? 2 : 3, (DH_P_BUDGET - WPW * NT * 16) / TILE_REGS));
     // Canonical NVFP4 layout: a loader warp streams each tile's scale bytes
     // into a shared-memory ring with 1-D bulk copies.
     static constexpr bool SCALES = (FMT == 1);

@@ -31,6 +31,9 @@ struct GemvArgs {
 // True if the draft-step kernels are compiled for (fmt, K).
 bool gemv_supported(int fmt, int K);
 
+// True if nvfp4_linear supports input width K (packed NVFP4 layout).
+bool linear_supported(int K);
+
 // Enqueue the GEMV + argmax (out == nullptr) or GEMV + logits scatter
 // (out != nullptr; the -inf fill must already be enqueued). Returns a
 // cudaError_t of the launch.

@@ -176,6 +176,23 @@ def test_activation_quantize_rejects_bad_arguments(L, args, status):
     assert L.fp8_quantize_activations(a["h"], a["M"], a["K"], a["qx"], a["sx"], None) == status
 
 
+@pytest.mark.parametrize("kw,M,status", [
+    (dict(), 0, dh.DH_ERR_SHAPE),
+    (dict(), 17, dh.DH_ERR_SHAPE),
+    (dict(fmt=dh.DH_FMT_NVFP4), 1, dh.DH_ERR_ARG),     # the packed layout only
+    (dict(K=384), 1, dh.DH_ERR_SHAPE),                 # no kernel for this input width
+    (dict(N=100), 1, dh.DH_ERR_SHAPE),                 # N % 64 != 0
+    (dict(scale=None), 1, dh.DH_ERR_ARG),
+    (dict(q=0x10008), 1, dh.DH_ERR_ALIGN),
+])
+def test_linear_rejects_bad_arguments(L, kw, M, status):
+    d = _desc(**dict(dict(fmt=dh.DH_FMT_NVFP4_PACKED, sf=None, idx=None, K=1024, N=256), **kw))
+    assert L.nvfp4_linear(C.byref(d), H, M, 0x500000, WS, 1 << 20, None) == status
+    d = _desc(fmt=dh.DH_FMT_NVFP4_PACKED, sf=None, idx=None, K=1024, N=256)
+    assert L.nvfp4_linear(C.byref(d), H, 1, 0x500008, WS, 1 << 20, None) == dh.DH_ERR_ALIGN
+    assert L.nvfp4_linear(C.byref(d), H, 1, 0x500000, WS, 64, None) == dh.DH_ERR_WORKSPACE
+
+
 def test_w8a8_head_descriptor_checks(L):
     d = _desc(fmt=dh.DH_FMT_FP8_W8A8, sf=None, scale=None)
     assert L.draft_head_top_tokens(C.byref(d), H, 1, 0x300000, None, WS, 256, None) == dh.DH_ERR_ARG

@@ -5,7 +5,8 @@
     gap < 1e-3 in 5 % of rows), both get_top_tokens and compute_logits;
   * the 98,304-row FP8 head: quantise bit-exact, M = 1 and 4, both paths,
     W8A16 and W8A8 (per-token FP8 hidden states);
-  * the full-vocabulary BF16 head (the stock drafter read) at M = 1.
+  * the full-vocabulary BF16 head (the stock drafter read) at M = 1;
+  * the truncated 40,960-row BF16 head (the FP8 page's draft_lm_head).
 The oracle computes every output here (its fp64 GEMV over a whole head takes
 about a second per draft row on one core)."""
 import numpy as np
@@ -16,7 +17,7 @@ import nvfp4_draft_head_gb300 as dh
 import oracle
 import synthetic as syn
 from parity_util import Workload, check_argmax_rows, check_logits, ids_to_rows, plant_near_ties
-from test_parity_gpu import dev, dev_bf16, pack_reference, run_step, run_step_w8a8
+from test_parity_gpu import check_step, dev, dev_bf16, pack_reference, run_step, run_step_w8a8
 
 pytestmark = pytest.mark.gpu
 
@@ -115,6 +116,18 @@ def test_fp8_98k_head(W_full, W_dev):
     for M in (1, 4):
         h = syn.hidden_bf16(syn.hidden_seed(2, 10 + M), M, wl.K)
         run_step_w8a8(w8a8, h, q_o, s_o, wl.idx, wl.n_kept, wl.V, f"fp8 w8a8 98k M={M}")
+
+
+def test_bf16_truncated_40960_head(W_full, W_dev):
+    """The FP8 page's truncated 40,960-row BF16 draft_lm_head, read in place
+    from the target head, M = 1 and 4, both paths."""
+    head = dh.bf16_truncated_head(W_dev, 40_960)
+    W_t = np.ascontiguousarray(W_full[:40_960])
+    idx = np.arange(40_960, dtype=np.int32)
+    for M in (1, 4):
+        h = syn.hidden_bf16(syn.hidden_seed(5, M), M, W_full.shape[1])
+        y, A = oracle.gemv(oracle.FMT_BF16, W_t, None, None, h)
+        check_step(head, h, y, A, idx, 40_960, W_full.shape[0], f"bf16 truncated 40,960 M={M}")
 
 
 def test_bf16_full_vocabulary_head(W_full, W_dev):

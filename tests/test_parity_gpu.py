@@ -216,6 +216,37 @@ def test_tiny_bf16_full_head_step(tiny, M):
     run_step(head, h, oracle.FMT_BF16, tiny.W, None, None, None, tiny.V, tiny.V, f"tiny bf16 M={M}")
 
 
+@pytest.mark.parametrize("N,K", [(128, 256), (192, 512), (1024, 1024), (640, 2048), (1024, 2560),
+                                 (320, 4096), (2560, 5120)])
+def test_nvfp4_linear(N, K):
+    """An MTP-block linear y = x W'^T (NVFP4 W4A16, fp32 out) at every supported
+    input width; N = 2560, K = 5120 is the fc projection of a 2560-wide block."""
+    W = syn.head_bf16(4000 + K, N, K)
+    lin = dh.NVFP4Linear(dev_bf16(W))
+    idx = np.arange(N, dtype=np.int32)
+    q_o, sf_o, g_o = oracle.nvfp4_quantize(W, idx)
+    assert np.array_equal(lin.q.cpu().numpy(), q_o) and np.array_equal(lin.sf.cpu().numpy(), sf_o)
+    assert np.array_equal(lin.packed.cpu().numpy(), pack_reference(q_o, sf_o))
+    for M in (1, 3, 16):
+        x = syn.hidden_bf16(4100 + M + K, M, K)
+        y = lin(dev_bf16(x)).cpu().numpy()
+        assert lin.device_error() == 0
+        y_o, A = oracle.gemv(oracle.FMT_NVFP4, q_o, sf_o, g_o, x)
+        check_logits(y, y_o, A, f"linear N={N} K={K} M={M}")
+
+
+@pytest.mark.parametrize("n_rows,M", [(4096, 1), (4096, 5), (64, 2), (16_384, 16)])
+def test_tiny_bf16_truncated_head_step(tiny, n_rows, M):
+    """The truncated BF16 draft head (the first n_rows ids of the target head):
+    argmax over those rows, -inf beyond them in compute_logits."""
+    head = dh.bf16_truncated_head(dev_bf16(tiny.W), n_rows)
+    h = syn.hidden_bf16(syn.hidden_seed(0, 800 + n_rows + M), M, tiny.K)
+    W_t = np.ascontiguousarray(tiny.W[:n_rows])
+    idx = np.arange(n_rows, dtype=np.int32)
+    y, A = oracle.gemv(oracle.FMT_BF16, W_t, None, None, h)
+    check_step(head, h, y, A, idx, n_rows, tiny.V, f"tiny bf16 truncated N={n_rows} M={M}")
+
+
 @pytest.mark.parametrize("V,K,n_kept,forced", [
     (64, 256, 1, 1),          # one kept id: N = 64, 63 padding rows
     (4096, 256, 4096, 0),     # every id kept: a plain full-vocabulary argmax
