@@ -50,7 +50,7 @@ STEP_BYTES = N_ROWS * (K_HID // 2) + N_ROWS * (K_HID // 16) + 4 + 2 * K_HID + 4
 # launches) of one launch of the M = 1 GEMV from the ncu capture summarised in
 # profiles/gemv_nvfp4_packed_m1_qwen64k.md; reported only while the kernel
 # sources still hash to kernel_sha (else null).
-TRAFFIC = {"kernel_sha": "334f9e3e2ba6e35d", "bytes_per_launch": 94_891_648}
+TRAFFIC = {"kernel_sha": "28580724f0e31aab", "bytes_per_launch": 94_882_944}
 
 
 def kernel_sha() -> str:
@@ -361,6 +361,50 @@ def run_ours(args, world, rank, local):
     del lib_loaded
 
 
+def run_profile_case(args):
+    """Eager draft steps of one secondary workload for a profiler (no timing,
+    no output but one line): the batch sweep on the NVFP4 head (--drafts M),
+    the 98,304-row FP8 head (W8A16 or W8A8), or the fc-sized NVFP4 linear."""
+    import torch
+
+    import nvfp4_draft_head_gb300 as dh
+    from nvfp4_draft_head_gb300 import build
+    build.build()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    M = args.drafts
+    hs = torch.from_numpy(np.concatenate([syn.hidden_bf16(7000 + i, 16, K_HID) for i in range(8)]).view(np.int16)
+                          ).to(dev).view(torch.bfloat16).reshape(8, 16, K_HID)
+    W, keep = workload_host()
+    Wd = torch.from_numpy(W.view(np.int16)).to(dev).view(torch.bfloat16)
+    del W
+    if args.profile_case == "nvfp4":
+        h0 = dh.nvfp4_head(Wd, keep)
+        units = [h0] + [h0.with_storage(h0.q.clone()) for _ in range(COPIES - 1)]
+    elif args.profile_case in ("fp8", "w8a8"):
+        c = syn.FP8_98K
+        k8 = syn.keep_mask(syn.SEED_KEEP_98K, c["V"], c["n_kept"], c["forced"])
+        h8 = dh.fp8_head(Wd, k8, w8a8=args.profile_case == "w8a8")
+        units = [h8] + [h8.with_storage(h8.q.clone()) for _ in range(2)]
+    else:  # linear: fc 5,120 -> 2,560, 70 copies (520 MB)
+        Wl = torch.from_numpy(syn.head_bf16(4000 + 5120, 2560, 5120).view(np.int16)).to(dev).view(torch.bfloat16)
+        l0 = dh.NVFP4Linear(Wl)
+        units = [l0] + [l0.with_storage(l0.packed.clone()) for _ in range(69)]
+        hs = torch.from_numpy(np.concatenate([syn.hidden_bf16(7200 + i, 16, 5120) for i in range(8)]).view(np.int16)
+                              ).to(dev).view(torch.bfloat16).reshape(8, 16, 5120)
+    del Wd
+    ids = torch.empty(M, dtype=torch.int32, device=dev)
+    for i in range(args.warmup + args.steps):
+        u = units[i % len(units)]
+        if args.profile_case == "linear":
+            u(hs[i % 8, :M])
+        else:
+            u.top_tokens(hs[i % 8, :M], ids=ids)
+    torch.cuda.synchronize()
+    assert units[0].device_error() == 0
+    emit({"profile_run": True, "case": args.profile_case, "drafts": M, "steps": args.steps, "warmup": args.warmup})
+
+
 def run_suite(args):
     """Secondary measurements (one JSON line each) of the other workloads:
     the FP8 98,304-row head, the batch sweep, the BF16 full-vocabulary head,
@@ -486,6 +530,23 @@ def run_suite(args):
         line(f"bf16 truncated 40,960 x 2560 top_tokens M={M}", graph_us(calls), 40_960 * K_HID * 2 + M * (2 * K_HID + 4),
              {"M": M})
 
+    # NVFP4 W4A16 MTP-block linears (synthetic shapes around a 2,560-wide block),
+    # each rotated over copies totalling > 4 x L2
+    for K_in, N_out, name in ((5120, 2560, "fc"), (2560, 4608, "qkv"), (4096, 2560, "o_proj"),
+                              (2560, 1024, "shared-expert gate/up"), (512, 2560, "shared-expert down")):
+        Wl = torch.from_numpy(syn.head_bf16(4000 + K_in, N_out, K_in).view(np.int16)).to(dev).view(torch.bfloat16)
+        l0 = dh.NVFP4Linear(Wl)
+        nb = N_out * (K_in // 2 + K_in // 16)
+        lins = [l0] + [l0.with_storage(l0.packed.clone()) for _ in range(max(1, (600 << 20) // nb) - 1)]
+        xs = torch.from_numpy(np.concatenate([syn.hidden_bf16(7200 + i, 16, K_in) for i in range(8)]).view(np.int16)
+                              ).to(dev).view(torch.bfloat16).reshape(8, 16, K_in)
+        for M in (1, 16):
+            y = torch.empty((M, N_out), dtype=torch.float32, device=dev)
+            calls = [(lambda i=i: lins[i % len(lins)](xs[i % 8, :M], y=y)) for i in range(steps)]
+            line(f"nvfp4 linear {name} {K_in}->{N_out} M={M}", graph_us(calls), nb + 4 + M * (2 * K_in + 4 * N_out),
+                 {"M": M, "copies": len(lins)})
+        del lins, l0, Wl
+
     # tiny head (L2-resident, latency-bound)
     ct = syn.TINY
     Wt = torch.from_numpy(syn.head_bf16(syn.SEED_HEAD_TINY, ct["V"], ct["K"]).view(np.int16)).to(dev).view(torch.bfloat16)
@@ -503,12 +564,19 @@ def main():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--profile", action="store_true",
                     help="eager steps only, for ncu (prints no measurement)")
+    ap.add_argument("--profile-case", choices=("nvfp4", "fp8", "w8a8", "linear"), default=None,
+                    help="with --profile: a secondary workload (NVFP4 head at --drafts M, the 98,304-row FP8 "
+                         "head W8A16 / W8A8, or the fc-sized NVFP4 linear)")
+    ap.add_argument("--drafts", type=int, default=1, help="drafts per step for --profile-case")
     ap.add_argument("--suite", action="store_true",
                     help="one line per secondary workload (FP8 head, batch sweep, BF16 head, head build, tiny)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     world, rank, local = dist_setup()
+    if args.profile and args.profile_case:
+        run_profile_case(args)
+        return
     if args.suite:
         run_suite(args)
         return

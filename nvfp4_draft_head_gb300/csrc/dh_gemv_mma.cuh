@@ -54,12 +54,10 @@
 namespace dh {
 namespace mma {
 
-#ifndef DH_P_BUDGET
-#define DH_P_BUDGET 64  // registers per thread for tile loads in flight plus the h fragments
-#endif
-#ifndef DH_NW_MAX
-#define DH_NW_MAX 20  // compute warps per CTA at most (fewer: several windows per warp, 2 CTAs per SM)
-#endif
+// Registers per thread for tile loads in flight plus the h fragments.
+constexpr int kLoadRegBudget = 64;
+// Compute warps per CTA at most.
+constexpr int kMaxComputeWarps = 20;
 
 constexpr int cmin(int a, int b) { return a < b ? a : b; }
 
@@ -79,7 +77,7 @@ constexpr int kIdCap = 48;
 template <int FMT, int K, int MT>
 struct Cfg {
     static constexpr int NWIN = K / 128;                     // 128-wide k-windows per row
-    static constexpr int NW = largest_divisor_at_most(NWIN, DH_NW_MAX);  // compute warps per CTA
+    static constexpr int NW = largest_divisor_at_most(NWIN, kMaxComputeWarps);  // compute warps per CTA
     static constexpr int WPW = NWIN / NW;                    // windows per warp
     static constexpr int NT = MT <= 8 ? 1 : 2;               // n8 tiles of drafts
     static constexpr bool NV = (FMT == 1 || FMT == 4);       // NVFP4 (canonical or packed layout)
@@ -97,7 +95,7 @@ struct Cfg {
     // fragments (16 registers per window and n8 tile), in the 80 registers that
     // 21+ warps per SM allow: three with one window per warp and one n8 tile,
     // two at 16 drafts, one with two windows per warp (K = 4096, 5120)
-    static constexpr int P = cmax(1, cmin(MT >= 16 ? 2 : 3, (DH_P_BUDGET - WPW * NT * 16) / TILE_REGS));
+    static constexpr int P = cmax(1, cmin(MT >= 16 ? 2 : 3, (kLoadRegBudget - WPW * NT * 16) / TILE_REGS));
     // Canonical NVFP4 layout: a loader warp streams each tile's scale bytes
     // into a shared-memory ring with 1-D bulk copies.
     static constexpr bool SCALES = (FMT == 1);
@@ -206,8 +204,7 @@ __device__ __forceinline__ uint32_t word_of(const uint4 (&v)[CPR], int i) {
 }
 
 template <int FMT, int K, int MT, bool LOGITS>
-__global__ void __launch_bounds__(Cfg<FMT, K, MT>::THREADS, Cfg<FMT, K, MT>::NW <= 10 ? 2 : 1)
-    gemv_mma_kernel(const GemvArgs a) {
+__global__ void __launch_bounds__(Cfg<FMT, K, MT>::THREADS, 1) gemv_mma_kernel(const GemvArgs a) {
     using C = Cfg<FMT, K, MT>;
     constexpr int NW = C::NW, WPW = C::WPW, NT = C::NT, P = C::P, KW = K / 2, RS = C::RS;
     constexpr int NRED = 16 * MT;  // (row, draft) results of a tile
@@ -227,9 +224,9 @@ __global__ void __launch_bounds__(Cfg<FMT, K, MT>::THREADS, Cfg<FMT, K, MT>::NW 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int g = lane >> 2, t = lane & 3;
     const int n_tiles = a.N / 16;
-    const int my_tiles = static_cast<int>(blockIdx.x) < n_tiles
-                             ? (n_tiles - 1 - static_cast<int>(blockIdx.x)) / static_cast<int>(gridDim.x) + 1
-                             : 0;
+    const int b0 = static_cast<int>(blockIdx.x);
+    const int my_tiles = b0 < n_tiles ? (n_tiles - 1 - b0) / static_cast<int>(gridDim.x) + 1 : 0;
+    auto tile_of = [&](int i) { return b0 + i * static_cast<int>(gridDim.x); };
     const uint8_t* q = static_cast<const uint8_t*>(a.q);
     volatile int* abort_flag = &s_abort;
 
@@ -238,7 +235,7 @@ __global__ void __launch_bounds__(Cfg<FMT, K, MT>::THREADS, Cfg<FMT, K, MT>::NW 
     if (warp < NW) {
 #pragma unroll
         for (int p = 0; p < P; ++p)
-            if (p < my_tiles) load_tile<FMT, K, MT>(buf[p], q, blockIdx.x + p * gridDim.x, warp, g, t);
+            if (p < my_tiles) load_tile<FMT, K, MT>(buf[p], q, tile_of(p), warp, g, t);
     }
 
     if (tid == 0) {
@@ -258,7 +255,7 @@ __global__ void __launch_bounds__(Cfg<FMT, K, MT>::THREADS, Cfg<FMT, K, MT>::NW 
     const uint64_t pol = policy_evict_first();
     auto issue = [&](int i) {
         const int slot = i % C::SS;
-        const size_t tile = static_cast<size_t>(blockIdx.x) + static_cast<size_t>(i) * gridDim.x;
+        const size_t tile = static_cast<size_t>(tile_of(i));
         mbar_arrive_expect_tx(&full_s[slot], C::SLOT);
         bulk_g2s(s_scales + slot * C::SLOT, a.sf + tile * C::SLOT, C::SLOT, &full_s[slot], pol);
     };
@@ -276,7 +273,7 @@ __global__ void __launch_bounds__(Cfg<FMT, K, MT>::THREADS, Cfg<FMT, K, MT>::NW 
     if (warp >= NW && warp < NW + C::NRW) {
         for (int c = (warp - NW) * 32 + lane; c < n_pre * 5; c += 32 * C::NRW) {
             const int i = c / 5, ch = c - 5 * i;  // 16-byte chunk ch of tile i: ids 16 tile + 4 ch ..
-            const size_t e = (static_cast<size_t>(blockIdx.x) + static_cast<size_t>(i) * gridDim.x) * 16 + 4 * ch;
+            const size_t e = static_cast<size_t>(tile_of(i)) * 16 + 4 * ch;
             if (e + 4 <= static_cast<size_t>(a.N)) cp_async16(&s_ids[20 * i + 4 * ch], a.idx + e);
         }
     }
@@ -327,7 +324,7 @@ __global__ void __launch_bounds__(Cfg<FMT, K, MT>::THREADS, Cfg<FMT, K, MT>::NW 
         constexpr int SLOTS = (NU + 32 * C::NRW - 1) / (32 * C::NRW);  // units per reducer thread
         for (int i = 0; i < my_tiles; ++i) {
             const int slot = i % RS;
-            const int tile = static_cast<int>(blockIdx.x) + i * static_cast<int>(gridDim.x);
+            const int tile = tile_of(i);
             const int r0 = tile * 16;
             // dh_idx of this tile's rows, fetched before waiting for the partials
             int ids_[SLOTS];
@@ -672,7 +669,7 @@ __global__ void __launch_bounds__(Cfg<FMT, K, MT>::THREADS, Cfg<FMT, K, MT>::NW 
                 }
                 // loads of the tile P steps ahead go into the buffer just consumed
                 const int tn = ti + P;
-                if (tn < my_tiles) load_tile<FMT, K, MT>(buf[p], q, blockIdx.x + tn * gridDim.x, warp, g, t);
+                if (tn < my_tiles) load_tile<FMT, K, MT>(buf[p], q, tile_of(tn), warp, g, t);
                 // hand the partials to the reducer (wait for the slot to be free first)
                 if (ti >= RS && !*abort_flag && !mbar_wait(&empty_p[slot], ((ti / RS) - 1) & 1)) {
                     atomicOr(&a.ws->error, kDevErrTimeout);
