@@ -124,6 +124,24 @@ def dist_setup():
     return world, rank, local
 
 
+def max_over_ranks(x: float, device) -> float:
+    """The largest of every rank's x (all-reduce MAX over the default process
+    group; x itself when there is no group)."""
+    import torch
+    import torch.distributed as tdist
+    if not (tdist.is_available() and tdist.is_initialized()) or tdist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_us_per_step(ms_max: float, steps: int, world: int) -> float:
+    """µs per draft step of the whole job: N replicas each ran `steps` steps in
+    at most ms_max milliseconds, so N * steps steps took ms_max."""
+    return ms_max * 1e3 / (steps * world)
+
+
 def workload_host():
     c = syn.QWEN_64K
     W = syn.head_bf16(syn.SEED_HEAD_QWEN, c["V"], c["K"])
@@ -289,9 +307,7 @@ def run_ours(args, world, rank, local):
         s.synchronize()
     clocks = sampler.stop()
     if world > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+        ms = max_over_ranks(ms, dev)
         torch.distributed.barrier()
     assert head.device_error() == 0
 
@@ -317,9 +333,7 @@ def run_ours(args, world, rank, local):
         torch.cuda.synchronize()
         ms_e2e = f0.elapsed_time(f1)
     if world > 1:
-        t = torch.tensor([ms_e2e], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_e2e = float(t.item())
+        ms_e2e = max_over_ranks(ms_e2e, dev)
     e2e_ok = bool(np.array_equal(ids_pin[Wm:].numpy(), ids[Wm:].cpu().numpy()))
 
     cpu = None
@@ -334,7 +348,7 @@ def run_ours(args, world, rank, local):
             torch.distributed.destroy_process_group()
         return
     us_step = ms * 1e3 / K
-    value = us_step / world
+    value = whole_job_us_per_step(ms, K, world)
     gbs = STEP_BYTES / (us_step * 1e-6) / 1e9
     peak, peak_src = hbm_peak()
     sha = kernel_sha()
@@ -352,7 +366,7 @@ def run_ours(args, world, rank, local):
                        "kernel": "gemv_mma_kernel<NVFP4 packed, K=2560, M=1> (top tokens)",
                        "bytes_per_launch": STEP_BYTES},
           "cpu_baseline": cpu,
-          "e2e": {"value": ms_e2e * 1e3 / K / world, "unit": "us/step", "h2d_bytes_per_step": 2 * K_HID,
+          "e2e": {"value": whole_job_us_per_step(ms_e2e, K, world), "unit": "us/step", "h2d_bytes_per_step": 2 * K_HID,
                   "d2h_bytes_per_step": 4, "ids_match_graph": e2e_ok},
           "gpu_launches": K, "clocks": clocks, "parity": parity,
           "library": os.path.relpath(dh.library_path(), ROOT), "kernel_sha": sha})

@@ -15,11 +15,16 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 // cudaError_t behind the calling thread's last DH_ERR_CUDA (0 if none yet).
 thread_local int t_last_cuda_error = 0;
 
-int cuda_status(cudaError_t e) {
-    if (e == cudaSuccess) return DH_OK;
+}  // namespace
+
+int dh::record_cuda_error(cudaError_t e) {
     t_last_cuda_error = static_cast<int>(e);
     return DH_ERR_CUDA;
 }
+
+namespace {
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? DH_OK : dh::record_cuda_error(e); }
 
 int check_ws(const void* ws, size_t ws_bytes, size_t need) {
     if (ws == nullptr) return DH_ERR_ARG;

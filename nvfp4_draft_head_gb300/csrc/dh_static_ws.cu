@@ -28,10 +28,14 @@ void* g_scratch_addr[kMaxDevices] = {nullptr};
 // per device (with that device current).
 int static_scratch(void** out) {
     int dev = -1;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return DH_ERR_CUDA;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return dh::record_cuda_error(e);
+    if (dev < 0 || dev >= kMaxDevices) return dh::record_cuda_error(cudaErrorInvalidDevice);
     if (g_scratch_addr[dev] == nullptr) {
         void* p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || p == nullptr) return DH_ERR_CUDA;
+        e = cudaGetSymbolAddress(&p, g_static_scratch);
+        if (e != cudaSuccess) return dh::record_cuda_error(e);
+        if (p == nullptr) return dh::record_cuda_error(cudaErrorInvalidSymbol);
         g_scratch_addr[dev] = p;
     }
     *out = g_scratch_addr[dev];
@@ -45,13 +49,16 @@ extern "C" int draft_head_top_tokens_static(const dh_head_t* hd, const void* h, 
     if (hd == nullptr || h == nullptr || ids == nullptr) return DH_ERR_ARG;
     if (M < 1 || M > DH_MAX_M) return DH_ERR_SHAPE;  // the scratch holds slots for 16 drafts
     if (hd->q == nullptr) return DH_ERR_ARG;
-    if (hd->fmt != DH_FMT_NVFP4 && hd->fmt != DH_FMT_FP8 && hd->fmt != DH_FMT_BF16 && hd->fmt != DH_FMT_NVFP4_PACKED)
+    if (hd->fmt != DH_FMT_NVFP4 && hd->fmt != DH_FMT_FP8 && hd->fmt != DH_FMT_BF16 && hd->fmt != DH_FMT_NVFP4_PACKED &&
+        hd->fmt != DH_FMT_FP8_W8A8)
         return DH_ERR_ARG;
     if (hd->V <= 0 || hd->N <= 0 || hd->n_kept < 1 || hd->n_kept > hd->N || hd->N % 64 != 0)
         return DH_ERR_SHAPE;
     if (!dh::gemv_supported(hd->fmt, hd->K)) return DH_ERR_SHAPE;
     if (hd->fmt == DH_FMT_NVFP4 && (hd->sf == nullptr || hd->scale == nullptr)) return DH_ERR_ARG;
-    if ((hd->fmt == DH_FMT_FP8 || hd->fmt == DH_FMT_NVFP4_PACKED) && hd->scale == nullptr) return DH_ERR_ARG;
+    if ((hd->fmt == DH_FMT_FP8 || hd->fmt == DH_FMT_NVFP4_PACKED || hd->fmt == DH_FMT_FP8_W8A8) &&
+        hd->scale == nullptr)
+        return DH_ERR_ARG;
     if (hd->idx == nullptr && (hd->fmt != DH_FMT_BF16 || hd->n_kept != hd->N || hd->N > hd->V))
         return DH_ERR_ARG;
     const uintptr_t al16 = reinterpret_cast<uintptr_t>(hd->q) | reinterpret_cast<uintptr_t>(h) |
@@ -81,5 +88,6 @@ extern "C" int draft_head_top_tokens_static(const dh_head_t* hd, const void* h, 
     a.ids = ids;
     a.top = top_logit;
     a.ws = static_cast<dh::Workspace*>(scratch);
-    return dh::launch_gemv(a, s) == cudaSuccess ? DH_OK : DH_ERR_CUDA;
+    const cudaError_t e = dh::launch_gemv(a, s);
+    return e == cudaSuccess ? DH_OK : dh::record_cuda_error(e);
 }

@@ -56,3 +56,26 @@ def test_static_scratch_entry_point_matches_workspace_entry_point():
     ids17 = torch.empty(17, dtype=torch.int32, device="cuda")
     assert L.draft_head_top_tokens_static(C.byref(head.desc), h17.data_ptr(), 17, ids17.data_ptr(),
                                           None, stream) == dh.DH_ERR_SHAPE
+
+
+def test_static_scratch_entry_point_runs_the_w8a8_head():
+    """The same comparison for the W8A8 FP8 head (hidden states quantised per
+    token inside the step), which shares the draft-step kernel family."""
+    from nvfp4_draft_head_gb300 import build
+    build.build()
+    L = dh.lib()
+    c = syn.TINY
+    W = syn.head_bf16(syn.SEED_HEAD_TINY, c["V"], c["K"])
+    keep = syn.keep_mask(syn.SEED_KEEP_TINY, c["V"], c["n_kept"], c["forced"])
+    Wd = torch.from_numpy(W.view(np.int16)).cuda().view(torch.bfloat16)
+    head = dh.fp8_head(Wd, keep, w8a8=True)
+    stream = torch.cuda.current_stream().cuda_stream
+    for call, M in enumerate((1, 7)):
+        hb = syn.hidden_bf16(syn.hidden_seed(0, 7100 + call), M, c["K"])
+        h = torch.from_numpy(hb.view(np.int16)).cuda().view(torch.bfloat16)
+        ids_ws = head.top_tokens(h)
+        ids_st = torch.full((M,), -7, dtype=torch.int32, device="cuda")
+        assert L.draft_head_top_tokens_static(C.byref(head.desc), h.data_ptr(), M, ids_st.data_ptr(),
+                                              None, stream) == dh.DH_OK
+        torch.cuda.synchronize()
+        assert np.array_equal(ids_ws.cpu().numpy(), ids_st.cpu().numpy()), call
