@@ -9,7 +9,10 @@
 //   FP8 head", "How it was built"): g = max(amax, 1e-12) / (6 * 448); per
 //   16-element block two lanes each hold 8 elements, the block amax is one
 //   warp shuffle; s = E4M3_RNE_sat(bamax / (6 g)); codes = E2M1_RNE(clamp(
-//   w / (dec(s) g), +-6)); a zero decoded scale gives signed zeros.
+//   w / (dec(s) g), +-6)); a zero decoded scale gives signed zeros. The
+//   element codes come from the hardware conversion cvt.rn.satfinite.e2m1x2
+//   (round to nearest even, saturating at +-6, which is the clamp; a negative
+//   quotient that rounds to zero keeps its sign).
 //   FP8 ("FP8 MTP draft stack for vLLM ...", _fp8_convert_draft_head):
 //   scale = max(amax, 1e-12) / 448; q = E4M3_RNE(clamp(w / scale, +-448)).
 // All divisions and products are IEEE round-to-nearest (explicit __fdiv_rn /
@@ -28,25 +31,84 @@ __device__ __forceinline__ float ld_amax(const Workspace* ws) {
     return amax < 1e-12f ? 1e-12f : amax;
 }
 
+// Chunks each thread has in flight: its dh_idx loads, then the dependent row
+// loads, are issued for kU grid-stride iterations before any arithmetic.
+constexpr int kU = 4;
+
+// Position (row n, chunk kc of the row) of a thread's current chunk c =
+// n * cpr + kc, advanced by the grid stride without dividing: the stride is
+// sq rows and sr chunks.
+template <typename I>
+struct ChunkPos {
+    I n;
+    int kc;
+    __device__ __forceinline__ void advance(I sq, int sr, int cpr) {
+        kc += sr;
+        n += sq;
+        if (kc >= cpr) {
+            kc -= cpr;
+            ++n;
+        }
+    }
+};
+
+// Gathered 16-byte chunks: for the kU chunks c0 + u * stride of this thread
+// (p = the position of c0), the chunk's row id (or -1 past the last row / for
+// an id outside [0, V), which is recorded) and its 8 BF16 values. I is the
+// chunk index type (32-bit when the head has fewer than 2^31 chunks).
+template <typename I>
+__device__ __forceinline__ void gather_chunks(const uint4* __restrict__ W, int V, int cpr, const int32_t* __restrict__ idx,
+                                              I N, ChunkPos<I> p, I sq, int sr, Workspace* ws, bool flag_bad,
+                                              int (&id)[kU], int (&kc)[kU], uint4 (&v)[kU]) {
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+        id[u] = p.n < N ? __ldg(idx + p.n) : -1;
+        kc[u] = p.kc;
+        if (p.n < N && (id[u] < 0 || id[u] >= V)) {
+            if (flag_bad) atomicOr(&ws->error, kDevErrIdx);
+            id[u] = -1;
+        }
+        p.advance(sq, sr, cpr);
+    }
+#pragma unroll
+    for (int u = 0; u < kU; ++u)
+        v[u] = id[u] >= 0 ? ld_stream_v4(W + static_cast<size_t>(id[u]) * cpr + kc[u]) : make_uint4(0, 0, 0, 0);
+}
+
+// Start position and stride (in rows and chunks) of this thread's chunks.
+template <typename I>
+__device__ __forceinline__ void chunk_start(int cpr, ChunkPos<I>& p, I& sq, int& sr) {
+    const I c0 = static_cast<I>(blockIdx.x) * kQThreads + threadIdx.x;
+    const I stride = static_cast<I>(gridDim.x) * kQThreads;
+    p.n = c0 / static_cast<I>(cpr);
+    p.kc = static_cast<int>(c0 % static_cast<I>(cpr));
+    sq = stride / static_cast<I>(cpr);
+    sr = static_cast<int>(stride % static_cast<I>(cpr));
+}
+
 // W rows are read as 16-byte chunks of 8 BF16; chunk c covers row c / (K/8).
+template <typename I>
 __global__ void __launch_bounds__(kQThreads)
 gather_amax_kernel(const uint4* __restrict__ W, int V, int K, const int32_t* __restrict__ idx,
                    int N, Workspace* ws) {
     const int cpr = K / 8;  // chunks per row
-    const size_t total = static_cast<size_t>(N) * cpr;
+    ChunkPos<I> p;
+    I sq;
+    int sr;
+    chunk_start<I>(cpr, p, sq, sr);
     float am = 0.0f;
-    for (size_t c = blockIdx.x * static_cast<size_t>(kQThreads) + threadIdx.x; c < total;
-         c += static_cast<size_t>(gridDim.x) * kQThreads) {
-        const int n = static_cast<int>(c / cpr), kc = static_cast<int>(c % cpr);
-        const int id = __ldg(idx + n);
-        if (id < 0 || id >= V) {
-            atomicOr(&ws->error, kDevErrIdx);
-            continue;
-        }
-        const uint4 v = ld_stream_v4(W + static_cast<size_t>(id) * cpr + kc);
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    for (; p.n < static_cast<I>(N);) {
+        int id[kU], kcs[kU];
+        uint4 v[kU];
+        gather_chunks<I>(W, V, cpr, idx, static_cast<I>(N), p, sq, sr, ws, true, id, kcs, v);
 #pragma unroll
-        for (int i = 0; i < 4; ++i) am = fmaxf(am, fmaxf(fabsf(bf16_lo(w[i])), fabsf(bf16_hi(w[i]))));
+        for (int u = 0; u < kU; ++u) p.advance(sq, sr, cpr);
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+            const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) am = fmaxf(am, fmaxf(fabsf(bf16_lo(w[i])), fabsf(bf16_hi(w[i]))));
+        }
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) am = fmaxf(am, __shfl_xor_sync(0xFFFFFFFFu, am, o));
@@ -60,16 +122,12 @@ gather_amax_kernel(const uint4* __restrict__ W, int V, int K, const int32_t* __r
     }
 }
 
-// E2M1 code of x (finite, already divided by the block's scale), round to
-// nearest with ties to the even code, saturating at 6; the sign bit follows
-// the sign of x. Thresholds are the midpoints of the E2M1 magnitudes
-// {0, .5, 1, 1.5, 2, 3, 4, 6}; ">" leaves a midpoint on the even code below
-// it and ">=" moves it to the even code above.
-__device__ __forceinline__ uint32_t e2m1_code(float x) {
-    const float a = fabsf(x);
-    uint32_t c = (a > 0.25f) + (a >= 0.75f) + (a > 1.25f) + (a >= 1.75f) + (a > 2.5f) +
-                 (a >= 3.5f) + (a > 5.0f);
-    return c | (signbit(x) ? 8u : 0u);
+// E2M1 codes of (lo, hi), lo in the low nibble: RNE, saturating at +-6.
+__device__ __forceinline__ uint32_t e2m1x2_code(float lo, float hi) {
+    uint32_t r;
+    asm("{\n\t.reg .b8 b;\n\tcvt.rn.satfinite.e2m1x2.f32 b, %1, %2;\n\tcvt.u32.u8 %0, b;\n\t}"
+        : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
 }
 
 __device__ __forceinline__ uint32_t e4m3_byte(float t) {
@@ -83,7 +141,9 @@ __device__ __forceinline__ float e4m3_value(uint32_t b) {
 
 // Two adjacent lanes share one 16-element block: the even lane holds elements
 // 0..7, the odd lane 8..15. Chunk indices of a pair are (2i, 2i+1) in the same
-// loop iteration because the grid stride is even.
+// loop iteration because the grid stride is even (and both lanes of a pair
+// see the same row, so they skip an invalid row together).
+template <typename I>
 __global__ void __launch_bounds__(kQThreads)
 nvfp4_encode_kernel(const uint4* __restrict__ W, int V, int K, const int32_t* __restrict__ idx,
                     int N, uint32_t* __restrict__ q, uint8_t* __restrict__ sf, float* g_out,
@@ -92,15 +152,25 @@ nvfp4_encode_kernel(const uint4* __restrict__ W, int V, int K, const int32_t* __
     const float den = __fmul_rn(6.0f, g);
     if (blockIdx.x == 0 && threadIdx.x == 0) *g_out = g;
     const int cpr = K / 8;
-    const size_t total = static_cast<size_t>(N) * cpr;
     const unsigned lane = threadIdx.x & 31;
     const unsigned pair = 3u << (lane & ~1u);
-    for (size_t c = blockIdx.x * static_cast<size_t>(kQThreads) + threadIdx.x; c < total;
-         c += static_cast<size_t>(gridDim.x) * kQThreads) {
-        const int n = static_cast<int>(c / cpr), kc = static_cast<int>(c % cpr);
-        const int id = __ldg(idx + n);
-        if (id < 0 || id >= V) continue;  // the amax pass has flagged it
-        const uint4 v = ld_stream_v4(W + static_cast<size_t>(id) * cpr + kc);
+    ChunkPos<I> p;
+    I sq;
+    int sr;
+    chunk_start<I>(cpr, p, sq, sr);
+    for (; p.n < static_cast<I>(N);) {
+      int ids[kU], kcs[kU];
+      uint4 vs[kU];
+      ChunkPos<I> pu = p;
+      gather_chunks<I>(W, V, cpr, idx, static_cast<I>(N), p, sq, sr, ws, false, ids, kcs, vs);  // amax pass flagged bad ids
+#pragma unroll
+      for (int u = 0; u < kU; ++u) p.advance(sq, sr, cpr);
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const I c = pu.n * static_cast<I>(cpr) + static_cast<I>(kcs[u]);
+        pu.advance(sq, sr, cpr);
+        if (ids[u] < 0) continue;
+        const uint4 v = vs[u];
         const uint32_t w[4] = {v.x, v.y, v.z, v.w};
         float x[8];
 #pragma unroll
@@ -115,36 +185,44 @@ nvfp4_encode_kernel(const uint4* __restrict__ W, int V, int K, const int32_t* __
         const uint32_t s = e4m3_byte(__fdiv_rn(bamax, den));
         const float d = __fmul_rn(e4m3_value(s), g);
         uint32_t packed = 0u;
+        if (d == 0.0f) {
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            uint32_t code;
-            if (d == 0.0f) {
-                code = signbit(x[i]) ? 8u : 0u;
-            } else {
-                float xi = __fdiv_rn(x[i], d);
-                xi = fminf(fmaxf(xi, -6.0f), 6.0f);
-                code = e2m1_code(xi);
-            }
-            packed |= code << (4 * i);
+            for (int i = 0; i < 8; ++i) packed |= (signbit(x[i]) ? 8u : 0u) << (4 * i);
+        } else {
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                packed |= e2m1x2_code(__fdiv_rn(x[2 * i], d), __fdiv_rn(x[2 * i + 1], d)) << (8 * i);
         }
         q[c] = packed;  // 8 codes = 4 bytes; chunk c starts at byte 4c of q
         if ((c & 1) == 0) sf[c >> 1] = static_cast<uint8_t>(s);
+      }
     }
 }
 
+template <typename I>
 __global__ void __launch_bounds__(kQThreads)
 fp8_encode_kernel(const uint4* __restrict__ W, int V, int K, const int32_t* __restrict__ idx,
                   int N, uint2* __restrict__ q, float* scale_out, Workspace* ws) {
     const float scale = __fdiv_rn(ld_amax(ws), 448.0f);
     if (blockIdx.x == 0 && threadIdx.x == 0) *scale_out = scale;
     const int cpr = K / 8;
-    const size_t total = static_cast<size_t>(N) * cpr;
-    for (size_t c = blockIdx.x * static_cast<size_t>(kQThreads) + threadIdx.x; c < total;
-         c += static_cast<size_t>(gridDim.x) * kQThreads) {
-        const int n = static_cast<int>(c / cpr), kc = static_cast<int>(c % cpr);
-        const int id = __ldg(idx + n);
-        if (id < 0 || id >= V) continue;
-        const uint4 v = ld_stream_v4(W + static_cast<size_t>(id) * cpr + kc);
+    ChunkPos<I> p;
+    I sq;
+    int sr;
+    chunk_start<I>(cpr, p, sq, sr);
+    for (; p.n < static_cast<I>(N);) {
+      int ids[kU], kcs[kU];
+      uint4 vs[kU];
+      ChunkPos<I> pu = p;
+      gather_chunks<I>(W, V, cpr, idx, static_cast<I>(N), p, sq, sr, ws, false, ids, kcs, vs);
+#pragma unroll
+      for (int u = 0; u < kU; ++u) p.advance(sq, sr, cpr);
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const I c = pu.n * static_cast<I>(cpr) + static_cast<I>(kcs[u]);
+        pu.advance(sq, sr, cpr);
+        if (ids[u] < 0) continue;
+        const uint4 v = vs[u];
         const uint32_t w[4] = {v.x, v.y, v.z, v.w};
         uint32_t b[8];
 #pragma unroll
@@ -156,6 +234,7 @@ fp8_encode_kernel(const uint4* __restrict__ W, int V, int K, const int32_t* __re
         }
         q[c] = make_uint2(b[0] | (b[1] << 8) | (b[2] << 16) | (b[3] << 24),
                           b[4] | (b[5] << 8) | (b[6] << 16) | (b[7] << 24));
+      }
     }
 }
 
@@ -201,6 +280,11 @@ cudaError_t launch_fp8_act_quantize(const uint16_t* h, int M, int K, uint8_t* qx
     return cudaGetLastError();
 }
 
+// 32-bit chunk indices suffice (with room for the unrolled strides).
+static bool small_index(int N, int K) {
+    return static_cast<unsigned long long>(N) * (K / 8) < (1ull << 31);
+}
+
 static int quant_blocks(int N, int K) {
     const size_t chunks = static_cast<size_t>(N) * (K / 8);
     const size_t want = (chunks + kQThreads - 1) / kQThreads;
@@ -215,10 +299,17 @@ cudaError_t launch_nvfp4_quantize(const uint16_t* W, int V, int K, const int32_t
     if (e != cudaSuccess) return e;
     const int blocks = quant_blocks(N, K);
     const uint4* W4 = reinterpret_cast<const uint4*>(W);
-    gather_amax_kernel<<<blocks, kQThreads, 0, s>>>(W4, V, K, idx, N, ws);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    nvfp4_encode_kernel<<<blocks, kQThreads, 0, s>>>(W4, V, K, idx, N,
-                                                      reinterpret_cast<uint32_t*>(q), sf, g, ws);
+    if (small_index(N, K)) {
+        gather_amax_kernel<uint32_t><<<blocks, kQThreads, 0, s>>>(W4, V, K, idx, N, ws);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        nvfp4_encode_kernel<uint32_t><<<blocks, kQThreads, 0, s>>>(W4, V, K, idx, N, reinterpret_cast<uint32_t*>(q),
+                                                                    sf, g, ws);
+    } else {
+        gather_amax_kernel<uint64_t><<<blocks, kQThreads, 0, s>>>(W4, V, K, idx, N, ws);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        nvfp4_encode_kernel<uint64_t><<<blocks, kQThreads, 0, s>>>(W4, V, K, idx, N, reinterpret_cast<uint32_t*>(q),
+                                                                    sf, g, ws);
+    }
     return cudaGetLastError();
 }
 
@@ -228,10 +319,17 @@ cudaError_t launch_fp8_quantize(const uint16_t* W, int V, int K, const int32_t* 
     if (e != cudaSuccess) return e;
     const int blocks = quant_blocks(N, K);
     const uint4* W4 = reinterpret_cast<const uint4*>(W);
-    gather_amax_kernel<<<blocks, kQThreads, 0, s>>>(W4, V, K, idx, N, ws);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    fp8_encode_kernel<<<blocks, kQThreads, 0, s>>>(W4, V, K, idx, N, reinterpret_cast<uint2*>(q),
-                                                    scale, ws);
+    if (small_index(N, K)) {
+        gather_amax_kernel<uint32_t><<<blocks, kQThreads, 0, s>>>(W4, V, K, idx, N, ws);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        fp8_encode_kernel<uint32_t><<<blocks, kQThreads, 0, s>>>(W4, V, K, idx, N, reinterpret_cast<uint2*>(q), scale,
+                                                                  ws);
+    } else {
+        gather_amax_kernel<uint64_t><<<blocks, kQThreads, 0, s>>>(W4, V, K, idx, N, ws);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        fp8_encode_kernel<uint64_t><<<blocks, kQThreads, 0, s>>>(W4, V, K, idx, N, reinterpret_cast<uint2*>(q), scale,
+                                                                  ws);
+    }
     return cudaGetLastError();
 }
 

@@ -114,6 +114,56 @@ def test_tiny_nvfp4_quantize_bit_exact(tiny):
     assert g.cpu().numpy()[0] == g_o
 
 
+def crafted_encoder_head():
+    """A 64 x 256 BF16 head whose NVFP4 quantisation meets every E2M1 decision.
+    Row 0 starts with 2688 (global amax, so g = 1 exactly); 181 blocks hold a
+    block maximum of 6 (block scale E4M3(1) = 1, so each quotient is the value
+    itself) and 15 values from a sweep of every BF16 value with magnitude in
+    [2^-8, 6.375] of both signs: every rounding midpoint (0.25 ... 5), the
+    values next to them, saturation (6 < x <= 6.375), plus signed zeros.
+    Remaining blocks are random."""
+    K, N = 256, 64
+    mags = []
+    for e in range(-8, 3):
+        for m in range(128):
+            v = np.float32((1 + m / 128) * 2.0 ** e)
+            if v <= 6.375:
+                mags.append(v)
+    mags = np.array(mags, np.float32)
+    sweep = np.concatenate([mags, -mags, np.float32([0.0, -0.0, 2.0 ** -12, -(2.0 ** -12)])])
+    W = syn.bf16_bits_to_f32(syn.head_bf16(31, N, K)).reshape(N, K // 16, 16)
+    W[0, 0, 0] = 2688.0
+    vals = iter(sweep)
+    blk = 1
+    done = False
+    while not done:
+        r, b = divmod(blk, K // 16)
+        W[r, b, 0] = 6.0
+        for j in range(1, 16):
+            v = next(vals, None)
+            if v is None:
+                done = True
+                W[r, b, j:] = 0.5
+                break
+            W[r, b, j] = v
+        blk += 1
+    return syn.f32_to_bf16_bits(W.reshape(N, K))
+
+
+def test_nvfp4_encoder_midpoints_signs_and_saturation():
+    Wb = crafted_encoder_head()
+    idx = np.arange(Wb.shape[0], dtype=np.int32)
+    q, sf, g = dh.nvfp4_quantize_rows(dev_bf16(Wb), dev(idx))
+    q_o, sf_o, g_o = oracle.nvfp4_quantize(Wb, idx)
+    assert g_o == 1.0 and g.cpu().numpy()[0] == g_o
+    assert np.array_equal(sf.cpu().numpy(), sf_o)
+    qg = q.cpu().numpy()
+    bad = np.argwhere(qg != q_o)
+    assert bad.size == 0, f"{len(bad)} code bytes differ, first (row, byte) {bad[:4].tolist()}"
+    # the sweep's blocks really decode with scale 1 (so the quotients are the values)
+    assert (sf_o.reshape(-1)[1:150] == 0x38).all()
+
+
 def test_tiny_fp8_quantize_bit_exact(tiny):
     _, (q, s) = gpu_fp8(tiny)
     q_o, s_o = tiny.fp8()
