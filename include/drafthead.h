@@ -242,6 +242,19 @@ int nvfp4_linear(const dh_head_t *w, const void *x, int M, float *y, void *ws, s
 int draft_head_top_tokens_static(const dh_head_t *hd, const void *h, int M, int32_t *ids,
                                  float *top_logit, void *stream);
 
+/* Self-test of the failure handling of the draft-step kernels (the pages have
+ * no counterpart): a one-thread kernel waits for an event that nothing
+ * produces and gives up after `rounds` tries, recording DH_DEVERR_TIMEOUT in
+ * the error word of `ws` exactly as a draft step whose wait ran out does; the
+ * context stays usable. kind 0: polls a word of the workspace header that
+ * nothing writes (the argmax hand-off's wait); kind 1: waits on a shared-memory
+ * mbarrier that nothing arrives on (the load pipeline's wait).
+ * ws: a workspace of at least draft_head_quantize_workspace_bytes() bytes;
+ * 1 <= rounds <= 2^22 (a draft step's own limit). Read the result with
+ * draft_head_read_device_error. Errors: DH_ERR_ARG (kind, rounds),
+ * DH_ERR_WORKSPACE. */
+int draft_head_wait_probe(void *ws, size_t ws_bytes, int kind, unsigned int rounds, void *stream);
+
 /* Synchronise `stream`, then read and clear the device error word of `ws`
  * (draft-step or quantiser workspace). *err = 0 when nothing was recorded. */
 int draft_head_read_device_error(void *ws, int *err, void *stream);

@@ -37,6 +37,7 @@ EXPORTS = (
     "draft_head_top_tokens", "draft_head_compute_logits", "draft_head_read_device_error",
     "draft_head_status_string", "draft_head_abi_version", "draft_head_top_tokens_static",
     "nvfp4_pack_head", "fp8_quantize_activations", "draft_head_last_cuda_error", "nvfp4_linear",
+    "draft_head_wait_probe",
 )
 
 _lib = None
@@ -93,6 +94,7 @@ def lib():
         L.fp8_quantize_activations.argtypes = [P, I, I, P, P, P]
         L.draft_head_last_cuda_error.argtypes = [C.POINTER(C.c_char_p)]
         L.nvfp4_linear.argtypes = [C.POINTER(dh_head_t), P, I, P, P, S, P]
+        L.draft_head_wait_probe.argtypes = [P, S, I, C.c_uint, P]
         _lib = L
     return _lib
 
@@ -199,6 +201,13 @@ def draft_head_read_device_error(ws: torch.Tensor, stream=None) -> int:
     _check("draft_head_read_device_error",
            lib().draft_head_read_device_error(ws.data_ptr(), C.byref(err), _stream(stream)))
     return err.value
+
+
+def draft_head_wait_probe(ws: torch.Tensor, kind: int, rounds: int, stream=None) -> None:
+    """Enqueue the bounded-wait self-test on workspace ws (kind 0: a global
+    word nothing writes, 1: an mbarrier nothing arrives on)."""
+    _check("draft_head_wait_probe",
+           lib().draft_head_wait_probe(ws.data_ptr(), ws.numel(), kind, rounds, _stream(stream)))
 
 
 def _raise_device_error(ws, stream, fn):

@@ -244,6 +244,15 @@ int nvfp4_linear(const dh_head_t* w, const void* x, int M, float* y, void* ws, s
     return cuda_status(dh::launch_gemv(a, static_cast<cudaStream_t>(stream)));
 }
 
+int draft_head_wait_probe(void* ws, size_t ws_bytes, int kind, unsigned int rounds, void* stream) {
+    int st = check_ws(ws, ws_bytes, dh::kWorkspaceHeader);
+    if (st != DH_OK) return st;
+    if (kind != 0 && kind != 1) return DH_ERR_ARG;
+    if (rounds < 1 || rounds > (1u << 22)) return DH_ERR_ARG;
+    return cuda_status(dh::launch_wait_probe(static_cast<dh::Workspace*>(ws), kind, rounds,
+                                             static_cast<cudaStream_t>(stream)));
+}
+
 int draft_head_read_device_error(void* ws, int* err, void* stream) {
     if (ws == nullptr || err == nullptr) return DH_ERR_ARG;
     if (!aligned(ws, DH_WORKSPACE_ALIGN)) return DH_ERR_WORKSPACE;

@@ -151,6 +151,7 @@ namespace dh {
 
 constexpr unsigned int kDevErrTimeout = 2u;   // a bounded pipeline wait gave up
 constexpr uint32_t kWaitLimit = 1u << 22;     // try_wait rounds before giving up
+constexpr uint32_t kSuspendNs = 1000;         // suspend-time hint of a try_wait round (ns)
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -174,18 +175,41 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" :: "r"(smem_u32(bar)) : "memory");
 }
 
-// Wait for the phase with the given parity to complete; false after kWaitLimit rounds.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+// Wait for the phase with the given parity to complete; false after `limit`
+// rounds. HINT: each try_wait round suspends for at most kSuspendNs, so that
+// `limit` rounds take a known time (kWaitLimit rounds ~ 4 s); without it a
+// round lasts a system-dependent time. (Measured: the hinted form is faster in
+// the one- and two-draft kernels, the plain form at 4 drafts and more.)
+template <bool HINT = true>
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t limit = kWaitLimit) {
     const uint32_t a = smem_u32(bar);
-    for (uint32_t i = 0; i < kWaitLimit; ++i) {
+    for (uint32_t i = 0; i < limit; ++i) {
         uint32_t done;
-        asm volatile("{\n\t.reg .pred p;\n\t"
-                     "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-                     "selp.u32 %0, 1, 0, p;\n\t}"
-                     : "=r"(done) : "r"(a), "r"(parity) : "memory");
+        if constexpr (HINT) {
+            asm volatile("{\n\t.reg .pred p;\n\t"
+                         "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+                         "selp.u32 %0, 1, 0, p;\n\t}"
+                         : "=r"(done) : "r"(a), "r"(parity), "n"(kSuspendNs) : "memory");
+        } else {
+            asm volatile("{\n\t.reg .pred p;\n\t"
+                         "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+                         "selp.u32 %0, 1, 0, p;\n\t}"
+                         : "=r"(done) : "r"(a), "r"(parity) : "memory");
+        }
         if (done) return true;
     }
     return false;
+}
+
+// Poll a 64-bit word in global memory (relaxed, device scope) until it is
+// non-zero; returns it, or 0 after `limit` polls.
+__device__ __forceinline__ unsigned long long poll_nonzero(const unsigned long long* p, uint32_t limit = kWaitLimit) {
+    unsigned long long v = 0ull;
+    for (uint32_t n = 0; n < limit; ++n) {
+        asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+        if (v != 0ull) break;
+    }
+    return v;
 }
 
 // Bulk copy global -> this CTA's shared memory, completing `bytes` on `bar`.

@@ -31,11 +31,7 @@ __device__ __forceinline__ void finish_argmax(const GemvArgs& a, const unsigned 
     for (int j = threadIdx.x; j < G * a.M; j += blockDim.x) {
         const int m = j / G, b = j - m * G;
         unsigned long long* p = &a.ws->slots[m][b];
-        unsigned long long v = 0ull;
-        for (uint32_t n = 0; n < kWaitLimit; ++n) {
-            asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
-            if (v != 0ull) break;
-        }
+        const unsigned long long v = poll_nonzero(p);
         if (v == 0ull) s_late = 1;
         asm volatile("st.relaxed.gpu.global.u64 [%0], 0;" :: "l"(p) : "memory");
         if (v > 1ull) atomicMax(&s_red[m], v);

@@ -24,6 +24,30 @@ __global__ void fill_neg_inf_kernel(float4* out4, size_t n4, float* tail, int nt
 }
 
 
+// Self-test of the bounded waits: wait for an event that never happens (kind
+// 0: a workspace word nothing writes, polled like the argmax hand-off's slots;
+// kind 1: an mbarrier nothing arrives on, waited on like the pipeline's), give
+// up after `rounds` and record DH_DEVERR_TIMEOUT, as the draft step does.
+__global__ void wait_probe_kernel(Workspace* ws, int kind, uint32_t rounds) {
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x != 0) return;
+    bool ok;
+    if (kind == 0) {
+        const unsigned long long* never = reinterpret_cast<const unsigned long long*>(&ws->pad_[0]);
+        ok = poll_nonzero(never, rounds) != 0ull;
+    } else {
+        mbar_init(&bar, 1);
+        mbar_init_fence();
+        ok = mbar_wait(&bar, 0, rounds);
+    }
+    if (!ok) atomicOr(&ws->error, kDevErrTimeout);
+}
+
+cudaError_t launch_wait_probe(Workspace* ws, int kind, uint32_t rounds, cudaStream_t s) {
+    wait_probe_kernel<<<1, 32, 0, s>>>(ws, kind, rounds);
+    return cudaGetLastError();
+}
+
 int sm_count() {
     static int cached[64] = {0};
     int dev = 0;

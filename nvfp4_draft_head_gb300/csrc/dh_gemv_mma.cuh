@@ -84,6 +84,7 @@ struct Cfg {
     static constexpr bool PACKED = (FMT == 4);                // tile-major NVFP4 layout
     static constexpr bool BLOCKDIAG = (NV && MT == 1);
     static constexpr bool W8A8 = (FMT == 5);                  // FP8 head, FP8 activations
+    static constexpr bool HINT = MT <= 2;                      // suspend-time hint on pipeline waits
     static constexpr int BPE2 = NV ? 1 : ((FMT == 2 || W8A8) ? 2 : 4);  // bytes per 2 elements
     static constexpr int RB = K * BPE2 / 2;                   // code bytes per head row
     static constexpr int WB = 128 * BPE2 / 2;                 // code bytes per row and window
@@ -292,7 +293,7 @@ __global__ void __launch_bounds__(Cfg<FMT, K, MT>::THREADS, 1) gemv_mma_kernel(c
             if (lane == 0) {
                 for (int i = issued; i < my_tiles; ++i) {
                     const int slot = i % C::SS;
-                    if (!mbar_wait(&empty_s[slot], ((i / C::SS) - 1) & 1)) {
+                    if (!mbar_wait<C::HINT>(&empty_s[slot], ((i / C::SS) - 1) & 1)) {
                         atomicOr(&a.ws->error, kDevErrTimeout);
                         *abort_flag = 1;
                     }
@@ -302,7 +303,7 @@ __global__ void __launch_bounds__(Cfg<FMT, K, MT>::THREADS, 1) gemv_mma_kernel(c
                 }
                 if (*abort_flag) {  // let the copies already issued land before the CTA exits
                     for (int i = issued > C::SS ? issued - C::SS : 0; i < issued; ++i)
-                        (void)mbar_wait(&full_s[i % C::SS], (i / C::SS) & 1);
+                        (void)mbar_wait<C::HINT>(&full_s[i % C::SS], (i / C::SS) & 1);
                 }
             }
             __syncwarp();
@@ -336,7 +337,7 @@ __global__ void __launch_bounds__(Cfg<FMT, K, MT>::THREADS, 1) gemv_mma_kernel(c
                               ? (i < n_pre ? s_ids[20 * i + u / UPR] : (a.idx ? __ldg(a.idx + row) : row))
                               : row;
             }
-            if (!*abort_flag && !mbar_wait(&full_p[slot], (i / RS) & 1)) {
+            if (!*abort_flag && !mbar_wait<C::HINT>(&full_p[slot], (i / RS) & 1)) {
                 atomicOr(&a.ws->error, kDevErrTimeout);
                 *abort_flag = 1;
             }
@@ -525,7 +526,7 @@ __global__ void __launch_bounds__(Cfg<FMT, K, MT>::THREADS, 1) gemv_mma_kernel(c
 
                 if constexpr (C::SCALES) {
                     const int ss = ti % C::SS;
-                    if (!*abort_flag && !mbar_wait(&full_s[ss], (ti / C::SS) & 1)) {
+                    if (!*abort_flag && !mbar_wait<C::HINT>(&full_s[ss], (ti / C::SS) & 1)) {
                         atomicOr(&a.ws->error, kDevErrTimeout);
                         *abort_flag = 1;
                     }
@@ -671,7 +672,7 @@ __global__ void __launch_bounds__(Cfg<FMT, K, MT>::THREADS, 1) gemv_mma_kernel(c
                 const int tn = ti + P;
                 if (tn < my_tiles) load_tile<FMT, K, MT>(buf[p], q, tile_of(tn), warp, g, t);
                 // hand the partials to the reducer (wait for the slot to be free first)
-                if (ti >= RS && !*abort_flag && !mbar_wait(&empty_p[slot], ((ti / RS) - 1) & 1)) {
+                if (ti >= RS && !*abort_flag && !mbar_wait<C::HINT>(&empty_p[slot], ((ti / RS) - 1) & 1)) {
                     atomicOr(&a.ws->error, kDevErrTimeout);
                     *abort_flag = 1;
                 }

@@ -57,6 +57,9 @@ cudaError_t launch_fp8_quantize(const uint16_t* W, int V, int K, const int32_t* 
 // qx [M][K] codes, sx [M] scales. One CTA per row.
 cudaError_t launch_fp8_act_quantize(const uint16_t* h, int M, int K, uint8_t* qx, float* sx, cudaStream_t s);
 
+// Bounded-wait self-test (kind 0: global-memory poll, 1: mbarrier wait).
+cudaError_t launch_wait_probe(Workspace* ws, int kind, uint32_t rounds, cudaStream_t s);
+
 // Remember e as the calling thread's last CUDA error (draft_head_last_cuda_error)
 // and return DH_ERR_CUDA.
 int record_cuda_error(cudaError_t e);

@@ -193,6 +193,15 @@ def test_linear_rejects_bad_arguments(L, kw, M, status):
     assert L.nvfp4_linear(C.byref(d), H, 1, 0x500000, WS, 64, None) == dh.DH_ERR_WORKSPACE
 
 
+def test_wait_probe_rejects_bad_arguments(L):
+    assert L.draft_head_wait_probe(None, 256, 0, 16, None) == dh.DH_ERR_ARG
+    assert L.draft_head_wait_probe(WS + 16, 256, 0, 16, None) == dh.DH_ERR_WORKSPACE
+    assert L.draft_head_wait_probe(WS, 128, 0, 16, None) == dh.DH_ERR_WORKSPACE
+    assert L.draft_head_wait_probe(WS, 256, 2, 16, None) == dh.DH_ERR_ARG
+    assert L.draft_head_wait_probe(WS, 256, 0, 0, None) == dh.DH_ERR_ARG
+    assert L.draft_head_wait_probe(WS, 256, 1, (1 << 22) + 1, None) == dh.DH_ERR_ARG
+
+
 def test_w8a8_head_descriptor_checks(L):
     d = _desc(fmt=dh.DH_FMT_FP8_W8A8, sf=None, scale=None)
     assert L.draft_head_top_tokens(C.byref(d), H, 1, 0x300000, None, WS, 256, None) == dh.DH_ERR_ARG

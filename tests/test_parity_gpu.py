@@ -374,6 +374,21 @@ def test_cuda_graph_replay(tiny):
         assert np.array_equal(ids, eager)
 
 
+@pytest.mark.parametrize("kind", [0, 1])
+def test_bounded_waits_give_up_and_report(tiny, kind):
+    """A wait for an event that never happens (a workspace word nothing writes;
+    an mbarrier nothing arrives on) gives up after its limit, sets the timeout
+    bit in the error word and leaves the context usable: the next draft step on
+    the same workspace is correct and reports no error."""
+    head, _ = gpu_nvfp4(tiny, packed=True)
+    dh.draft_head_wait_probe(head.ws, kind, 1 << 14 if kind == 0 else 1 << 11)
+    assert head.device_error() == dh.DH_DEVERR_TIMEOUT
+    assert head.device_error() == 0
+    q_o, sf_o, g_o = tiny.nvfp4()
+    h = syn.hidden_bf16(syn.hidden_seed(0, 4242 + kind), 2, tiny.K)
+    run_step(head, h, oracle.FMT_NVFP4, q_o, sf_o, g_o, tiny.idx, tiny.n_kept, tiny.V, f"after probe {kind}")
+
+
 def test_out_of_range_idx_sets_the_error_word(tiny):
     head, (q, sf, g) = gpu_nvfp4(tiny)
     bad = tiny.idx.copy()
