@@ -54,6 +54,7 @@
 namespace dh {
 namespace mma {
 
+
 // Registers per thread for tile loads in flight plus the h fragments.
 constexpr int kLoadRegBudget = 64;
 // Compute warps per CTA at most.
@@ -85,6 +86,11 @@ struct Cfg {
     static constexpr bool BLOCKDIAG = (NV && MT == 1);
     static constexpr bool W8A8 = (FMT == 5);                  // FP8 head, FP8 activations
     static constexpr bool HINT = MT <= 2;                      // suspend-time hint on pipeline waits
+    // tiles per CTA at least: 2 for the packed NVFP4 head at K <= 512, whose short
+    // tiles leave the step latency-bound (fewer CTAs to hand the argmax over);
+    // measured slower for K >= 2560 linears and no better for the FP8 head
+    static constexpr int MIN_TILES = (PACKED && K <= 512) ? 2 : 1;
+
     static constexpr int BPE2 = NV ? 1 : ((FMT == 2 || W8A8) ? 2 : 4);  // bytes per 2 elements
     static constexpr int RB = K * BPE2 / 2;                   // code bytes per head row
     static constexpr int WB = 128 * BPE2 / 2;                 // code bytes per row and window
@@ -738,6 +744,7 @@ inline cudaError_t launch_mma(const GemvArgs& a, cudaStream_t s) {
     const int n_tiles = a.N / 16;
     int blocks = sms * occ[dev];
     if (blocks > n_tiles) blocks = n_tiles;
+    if (blocks > (n_tiles + C::MIN_TILES - 1) / C::MIN_TILES) blocks = (n_tiles + C::MIN_TILES - 1) / C::MIN_TILES;
     if (blocks > kMaxGrid) blocks = kMaxGrid;  // one argmax slot per CTA
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(blocks);
