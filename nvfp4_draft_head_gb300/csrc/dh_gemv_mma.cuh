@@ -12,7 +12,7 @@
 // Work split. A tile is 16 head rows x the whole K. One CTA of NW warps owns a
 // tile at a time (tiles blockIdx.x, blockIdx.x + grid, ...); warp w owns the
 // 128-wide k-windows w, w + NW, ... of every tile, so its slice of h stays in
-// registers for the whole kernel. Thread (g = lane/4, t = lane%4) loads, for
+// registers for the whole kernel (in shared memory at 4 and 8 drafts). Thread (g = lane/4, t = lane%4) loads, for
 // head rows g and g+8 of the tile, the 32 consecutive k of each of its windows
 // starting at 32 t (one 16-byte load per row for NVFP4). Loads of the next
 // P-1 tiles are in flight while a tile is computed. Per-warp partial logits go
@@ -37,8 +37,9 @@
 // W8A8 FP8 head ("FP8 MTP draft stack for vLLM ...", _Fp8DraftHeadMethod.apply:
 // per-token dynamic E4M3 activations, scaled FP8 matmul). The compute warps
 // quantise h themselves: each finds the max |h| of its windows per draft, the
-// CTA's compute warps combine them in shared memory, and every thread encodes
-// its own 32 k of each draft (the codes are the B fragments). The multiply-adds
+// CTA's compute warps combine them in shared memory, and each warp encodes
+// every live draft's 128 values of its window together (4 per lane), then
+// hands each lane the 32 codes of its own k range (its B fragments). The multiply-adds
 // are mma.sync m16n8k32 e4m3 x e4m3 -> f32 on the raw codes (products of two
 // E4M3 values are exact in f32); a draft's partials are scaled by its
 // activation scale, the reducer's sum by the head's scale.
@@ -53,7 +54,6 @@
 
 namespace dh {
 namespace mma {
-
 
 // Registers per thread for tile loads in flight plus the h fragments.
 constexpr int kLoadRegBudget = 64;
@@ -98,15 +98,16 @@ struct Cfg {
     static constexpr int SFB = NV ? K / 16 : 0;               // scale bytes per head row
     static constexpr int WBLK = 16 * WB + 16 * 8;             // packed: bytes of one (tile, window) block
     static constexpr int TILE_REGS = WPW * (8 * CPR + (NV ? 4 : 0));
+    // NVFP4 at 4 and 8 drafts: the B fragments (h) come from shared memory (one
+    // 8-byte load per MMA) instead of 16 registers: 22.1 -> 21.9 and 24.6 -> 23.7
+    // µs per step. Slower at 2 drafts (+0.5 µs) and at 16 (+2.3 µs with two
+    // tiles in flight; spills with three). Packed layout only: the canonical
+    // layout's scale ring owns the dynamic shared memory.
+    static constexpr bool SMB = PACKED && !BLOCKDIAG && WPW == 1 && (MT == 4 || MT == 8);
     // tiles of loads in flight in registers: as many as fit, next to the h
     // fragments (16 registers per window and n8 tile), in the 80 registers that
     // 21+ warps per SM allow: three with one window per warp and one n8 tile,
     // two at 16 drafts, one with two windows per warp (K = 4096, 5120)
-    // NVFP4 at 8 drafts: the B fragments (h) come from shared memory (one 8-byte
-    // load per MMA) instead of 16 registers: 24.6 -> 23.7 µs per step. At 16
-    // drafts the same change spills with three tiles in flight (38 µs).
-    // (Packed layout only: the canonical layout's scale ring owns the dynamic shared memory.)
-    static constexpr bool SMB = PACKED && !BLOCKDIAG && MT == 8 && WPW == 1;
     static constexpr int P = SMB ? 3 : cmax(1, cmin(MT >= 16 ? 2 : 3, (kLoadRegBudget - WPW * NT * 16) / TILE_REGS));
     // Canonical NVFP4 layout: a loader warp streams each tile's scale bytes
     // into a shared-memory ring with 1-D bulk copies.
