@@ -339,6 +339,49 @@ def test_special_hidden_states(tiny):
     assert ids[0] == tiny.idx[0]
 
 
+@pytest.mark.parametrize("fmt", ["nvfp4_packed", "nvfp4_canonical", "fp8", "fp8_rowkeys", "w8a8", "bf16_full"])
+@pytest.mark.parametrize("M", [1, 5, 16])
+def test_exact_ties_resolve_to_the_lowest_id(tiny, fmt, M):
+    """Three kept rows in different tiles (and CTAs) carry identical weights that
+    dominate every draft's logits, so their quantised codes and logits are
+    exactly equal: each draft must return the lowest of the three ids (the
+    first maximum, as torch.argmax), whether the argmax keys carry ids or rows."""
+    W = tiny.W.copy()
+    kept = tiny.idx[: tiny.n_kept]
+    dup = [int(kept[3]), int(kept[len(kept) // 2]), int(kept[-2])]
+    h = np.repeat(syn.hidden_bf16(syn.hidden_seed(0, 7777), 1, tiny.K), M, axis=0)
+    hv = syn.bf16_bits_to_f32(h[0])
+    pattern = syn.f32_to_bf16_bits((0.25 * np.sign(hv)).astype(np.float32))
+    for i in dup:
+        W[i] = pattern
+    if fmt == "bf16_full":
+        head = dh.bf16_full_head(dev_bf16(W))
+        ids = head.top_tokens(dev_bf16(h)).cpu().numpy()
+        assert (ids == min(dup)).all(), ids
+        return
+    idx_d = dev(tiny.idx)
+    Wd = dev_bf16(W)
+    if fmt.startswith("nvfp4"):
+        q, sf, g = dh.nvfp4_quantize_rows(Wd, idx_d)
+        if fmt == "nvfp4_packed":
+            head = dh.DraftHead(dh.DH_FMT_NVFP4_PACKED, tiny.V, dh.nvfp4_pack_head(q, sf), idx_d, tiny.n_kept,
+                                scale=g, idx_ascending=True)
+        else:
+            head = dh.DraftHead(dh.DH_FMT_NVFP4, tiny.V, q, idx_d, tiny.n_kept, sf=sf, scale=g)
+    else:
+        q, s8 = dh.fp8_quantize_rows(Wd, idx_d)
+        f = dh.DH_FMT_FP8_W8A8 if fmt == "w8a8" else dh.DH_FMT_FP8
+        head = dh.DraftHead(f, tiny.V, q, idx_d, tiny.n_kept, scale=s8, idx_ascending=(fmt != "fp8_rowkeys"))
+    top = torch.empty(M, dtype=torch.float32, device="cuda")
+    ids = head.top_tokens(dev_bf16(h), top=top).cpu().numpy()
+    assert head.device_error() == 0
+    assert (ids == min(dup)).all(), (fmt, M, ids, dup)
+    # compute_logits writes the three equal logits at their own ids
+    out = head.compute_logits(dev_bf16(h)).cpu().numpy()
+    assert (out[:, dup[0]] == out[:, dup[1]]).all() and (out[:, dup[1]] == out[:, dup[2]]).all()
+    assert np.allclose(out[:, dup[0]], top.cpu().numpy())
+
+
 def test_same_hidden_rows_agree(tiny):
     head, _ = gpu_nvfp4(tiny)
     h = np.repeat(syn.hidden_bf16(11, 1, tiny.K), 6, axis=0)
