@@ -204,6 +204,14 @@ def oracle_all_cores(q, sf, g, hs, budget_s=10.0):
     return t_total / done, done, n_thr
 
 
+def bench_config(world: int) -> dict:
+    """The workload description both arms print."""
+    return {"workload": WORKLOAD, "M": 1, "V": 248_320, "K": K_HID, "N": N_ROWS, "n_kept": 64_026,
+            "head_copies": COPIES, "l2": "inputs larger than L2: 6 rotating head copies (553.5 MB > 4 x 129 MB)",
+            "timing": "one CUDA graph of K steps, CUDA events",
+            "parallelism": "replicas" if world > 1 else "single"}
+
+
 def emit(obj):
     print(json.dumps(obj), flush=True)
 
@@ -228,8 +236,7 @@ def run_reference(args, world, rank):
     emit({"impl": "reference", "metric": METRIC, "value": us, "unit": "us/step", "n_gpus": world,
           "steps": done, "warmup": args.warmup, "ms_per_step": us / 1e3, "higher_is_better": False,
           "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-          "config": {"workload": WORKLOAD, "M": 1, "V": 248_320, "K": K_HID, "N": N_ROWS,
-                     "n_kept": nk},
+          "config": bench_config(world),
           "cpu_baseline": cpu,
           "e2e": {"value": us, "unit": "us/step", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}})
 
@@ -389,10 +396,7 @@ def run_ours(args, world, rank, local):
     emit({"metric": METRIC, "value": value, "unit": "us/step", "n_gpus": world, "steps": K, "warmup": Wm,
           "ms_per_step": us_step / 1e3, "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
           "dtype": "f32", "data": "synthetic",
-          "config": {"workload": WORKLOAD, "M": 1, "V": 248_320, "K": K_HID, "N": N_ROWS, "n_kept": 64_026,
-                     "head_copies": COPIES, "l2": "inputs larger than L2: 6 rotating head copies "
-                     "(553.5 MB > 4 x 129 MB)", "timing": "one CUDA graph of K steps, CUDA events",
-                     "parallelism": "replicas" if world > 1 else "single"},
+          "config": bench_config(world),
           "hbm_gbs": gbs,
           "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "peak_source": peak_src,
                        "unit": "GB/s", "frac": gbs / peak, "traffic": traffic,
