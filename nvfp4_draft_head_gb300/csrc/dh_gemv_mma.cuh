@@ -423,11 +423,16 @@ __global__ void __launch_bounds__(Cfg<FMT, K, MT>::THREADS, 1) gemv_mma_kernel(c
 #pragma unroll
                 for (int ww = 0; ww < WPW; ++ww) {
                     const int k0 = 128 * (warp + ww * NW) + 32 * t;
+                    // the max |h| of this thread's 32 values (16-byte loads; the codes
+                    // are made from a second read below): W8A8 4 drafts 42.3 -> 41.2 µs,
+                    // 16 drafts 53.4 -> 50.6 µs against 4-byte loads
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        const uint32_t w = live ? __ldg(h32 + d * KW + k0 / 2 + j) : 0u;
-                        hb[ww][nt][j] = w;
-                        am = fmaxf(am, fmaxf(fabsf(bf16_lo(w)), fabsf(bf16_hi(w))));
+                    for (int j4 = 0; j4 < 4; ++j4) {
+                        const uint4 v = live ? __ldg(reinterpret_cast<const uint4*>(h32 + d * KW + k0 / 2) + j4)
+                                             : make_uint4(0u, 0u, 0u, 0u);
+                        const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) am = fmaxf(am, fmaxf(fabsf(bf16_lo(w4[j])), fabsf(bf16_hi(w4[j]))));
                     }
                 }
                 am = fmaxf(am, __shfl_xor_sync(0xFFFFFFFFu, am, 1));
@@ -460,7 +465,8 @@ __global__ void __launch_bounds__(Cfg<FMT, K, MT>::THREADS, 1) gemv_mma_kernel(c
 #pragma unroll
                 for (int ww = 0; ww < WPW; ++ww) {
                     const int kw = (128 * (warp + ww * NW) + 4 * lane) / 2;  // u32 index of the lane's 4 values
-                    const uint32_t w0 = __ldg(h32 + d * KW + kw), w1 = __ldg(h32 + d * KW + kw + 1);
+                    const uint2 v2 = __ldg(reinterpret_cast<const uint2*>(h32 + d * KW + kw));
+                    const uint32_t w0 = v2.x, w1 = v2.y;
                     const uint32_t word = act_fp8_pair(w0, sx) | (act_fp8_pair(w1, sx) << 16);
 #pragma unroll
                     for (int j = 0; j < 8; ++j) {
