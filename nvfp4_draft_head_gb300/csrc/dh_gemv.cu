@@ -15,6 +15,10 @@ bool linear_extra_k(int K);
 cudaError_t launch_linear_nvfp4_packed_extra(const GemvArgs& a, cudaStream_t s);
 
 __global__ void fill_neg_inf_kernel(float4* out4, size_t n4, float* tail, int ntail) {
+    // The GEMV launched next (programmatic stream serialisation) may start streaming
+    // the head now; it waits for this grid to complete before it touches `out`
+    // (compute_logits 16 drafts 30.6 -> 29.2 µs, one draft 22.0 -> 21.8 µs).
+    asm volatile("griddepcontrol.launch_dependents;");
     const float ninf = __uint_as_float(0xFF800000u);
     const float4 v = make_float4(ninf, ninf, ninf, ninf);
     for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n4;
