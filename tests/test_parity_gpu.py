@@ -432,6 +432,69 @@ def test_bounded_waits_give_up_and_report(tiny, kind):
     run_step(head, h, oracle.FMT_NVFP4, q_o, sf_o, g_o, tiny.idx, tiny.n_kept, tiny.V, f"after probe {kind}")
 
 
+@pytest.mark.parametrize("path", ["nvfp4_logits", "w8a8_top", "w8a8_logits", "linear"])
+def test_cuda_graph_replay_other_paths(tiny, path):
+    """compute_logits (fill kernel + GEMV), the W8A8 step and the MTP-block linear
+    are captured once and replayed with fresh inputs: each replay equals the
+    eager call and stays within the oracle's tolerance."""
+    M = 3
+    if path == "linear":
+        N, K = 256, 512
+        W = syn.head_bf16(4321, N, K)
+        lin = dh.NVFP4Linear(dev_bf16(W))
+        q_o, sf_o, g_o = oracle.nvfp4_quantize(W, np.arange(N, dtype=np.int32))
+        run = lambda x, y: lin(x, y=y)
+        out_shape, kdim = (M, N), K
+    else:
+        if path == "nvfp4_logits":
+            head, _ = gpu_nvfp4(tiny, packed=True)
+        else:
+            _, (q8, s8) = gpu_fp8(tiny)
+            head = dh.DraftHead(dh.DH_FMT_FP8_W8A8, tiny.V, q8, dev(tiny.idx), tiny.n_kept, scale=s8,
+                                idx_ascending=True)
+        if path.endswith("logits"):
+            run = lambda x, y: head.compute_logits(x, out=y)
+            out_shape = (M, tiny.V)
+        else:
+            run = lambda x, y: head.top_tokens(x, ids=y)
+            out_shape = (M,)
+        kdim = tiny.K
+    x_static = torch.zeros((M, kdim), dtype=torch.bfloat16, device="cuda")
+    dtype = torch.int32 if path == "w8a8_top" else torch.float32
+    y_static = torch.empty(out_shape, dtype=dtype, device="cuda")
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        run(x_static, y_static)                            # warm-up outside capture
+    torch.cuda.current_stream().wait_stream(s)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        run(x_static, y_static)
+    for step in range(3):
+        hb = syn.hidden_bf16(syn.hidden_seed(0, 9100 + 10 * step), M, kdim)
+        x_static.copy_(dev_bf16(hb))
+        graph.replay()
+        got = y_static.cpu().numpy().copy()
+        eager = run(dev_bf16(hb), torch.empty_like(y_static)).cpu().numpy()
+        assert np.array_equal(got, eager), (path, step)
+        if path == "linear":
+            y_o, A = oracle.gemv(oracle.FMT_NVFP4, q_o, sf_o, g_o, hb)
+            check_logits(got, y_o, A, f"graph linear {step}")
+        elif path == "w8a8_top":
+            qx, sx = oracle.fp8_act_quantize(hb)
+            y_o, A = oracle.gemv_w8a8(*tiny.fp8(), qx, sx)
+            check_argmax_rows(ids_to_rows(got, tiny.idx, tiny.n_kept), y_o, A, tiny.n_kept, f"graph w8a8 {step}")
+        else:
+            if path == "w8a8_logits":
+                qx, sx = oracle.fp8_act_quantize(hb)
+                y_o, A = oracle.gemv_w8a8(*tiny.fp8(), qx, sx)
+            else:
+                y_o, A = oracle.gemv(oracle.FMT_NVFP4, *tiny.nvfp4(), hb)
+            kept = tiny.idx[: tiny.n_kept]
+            check_logits(got[:, kept], y_o[:, : tiny.n_kept], A[:, : tiny.n_kept], f"graph {path} {step}")
+            assert np.isneginf(np.delete(got, kept, axis=1)).all()
+
+
 def test_out_of_range_idx_sets_the_error_word(tiny):
     head, (q, sf, g) = gpu_nvfp4(tiny)
     bad = tiny.idx.copy()
