@@ -41,7 +41,11 @@ int check_gather(const void* W, int V, int K, const int32_t* idx, int N) {
     return DH_OK;
 }
 
-int check_head(const dh_head_t* hd) {
+}  // namespace
+
+// Checks and argument block shared by every draft-step entry point (including
+// the static-scratch one in dh_static_ws.cu).
+static int check_head(const dh_head_t* hd) {
     if (hd == nullptr || hd->q == nullptr) return DH_ERR_ARG;
     if (hd->fmt != DH_FMT_NVFP4 && hd->fmt != DH_FMT_FP8 && hd->fmt != DH_FMT_BF16 && hd->fmt != DH_FMT_NVFP4_PACKED &&
         hd->fmt != DH_FMT_FP8_W8A8)
@@ -62,7 +66,7 @@ int check_head(const dh_head_t* hd) {
     return DH_OK;
 }
 
-int check_step(const dh_head_t* hd, const void* h, int M) {
+int dh::check_step_args(const dh_head_t* hd, const void* h, int M) {
     int st = check_head(hd);
     if (st != DH_OK) return st;
     if (h == nullptr) return DH_ERR_ARG;
@@ -71,7 +75,7 @@ int check_step(const dh_head_t* hd, const void* h, int M) {
     return DH_OK;
 }
 
-dh::GemvArgs make_args(const dh_head_t* hd, const void* h, int M, void* ws) {
+dh::GemvArgs dh::step_args(const dh_head_t* hd, const void* h, int M, void* ws) {
     dh::GemvArgs a;
     std::memset(&a, 0, sizeof a);
     a.fmt = hd->fmt;
@@ -89,8 +93,6 @@ dh::GemvArgs make_args(const dh_head_t* hd, const void* h, int M, void* ws) {
     a.ws = static_cast<dh::Workspace*>(ws);
     return a;
 }
-
-}  // namespace
 
 extern "C" {
 
@@ -191,12 +193,12 @@ int draft_head_workspace_init(void* ws, size_t ws_bytes, void* stream) {
 
 int draft_head_top_tokens(const dh_head_t* hd, const void* h, int M, int32_t* ids, float* top_logit,
                           void* ws, size_t ws_bytes, void* stream) {
-    int st = check_step(hd, h, M);
+    int st = dh::check_step_args(hd, h, M);
     if (st != DH_OK) return st;
     if (ids == nullptr) return DH_ERR_ARG;
     if (!aligned(ids, 4) || (top_logit && !aligned(top_logit, 4))) return DH_ERR_ALIGN;
     if ((st = check_ws(ws, ws_bytes, sizeof(dh::Workspace))) != DH_OK) return st;
-    dh::GemvArgs a = make_args(hd, h, M, ws);
+    dh::GemvArgs a = dh::step_args(hd, h, M, ws);
     a.ids = ids;
     a.top = top_logit;
     return cuda_status(dh::launch_gemv(a, static_cast<cudaStream_t>(stream)));
@@ -204,13 +206,13 @@ int draft_head_top_tokens(const dh_head_t* hd, const void* h, int M, int32_t* id
 
 int draft_head_compute_logits(const dh_head_t* hd, const void* h, int M, float* out, void* ws,
                               size_t ws_bytes, void* stream) {
-    int st = check_step(hd, h, M);
+    int st = dh::check_step_args(hd, h, M);
     if (st != DH_OK) return st;
     if (out == nullptr) return DH_ERR_ARG;
     if (!aligned(out, 16)) return DH_ERR_ALIGN;
     if ((st = check_ws(ws, ws_bytes, sizeof(dh::Workspace))) != DH_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    dh::GemvArgs a = make_args(hd, h, M, ws);
+    dh::GemvArgs a = dh::step_args(hd, h, M, ws);
     a.out = out;
     cudaError_t e = dh::launch_fill_neg_inf(out, static_cast<size_t>(M) * hd->V, s);
     if (e != cudaSuccess) return cuda_status(e);

@@ -60,6 +60,12 @@ cudaError_t launch_fp8_act_quantize(const uint16_t* h, int M, int K, uint8_t* qx
 // Bounded-wait self-test (kind 0: global-memory poll, 1: mbarrier wait).
 cudaError_t launch_wait_probe(Workspace* ws, int kind, uint32_t rounds, cudaStream_t s);
 
+// Host-side checks of a draft-step call (head descriptor, h, 1 <= M <= 16):
+// DH_OK or the dh_status to return; and the kernel arguments of the call
+// (ids, top and out left empty).
+int check_step_args(const struct dh_head* hd, const void* h, int M);
+GemvArgs step_args(const struct dh_head* hd, const void* h, int M, void* ws);
+
 // Remember e as the calling thread's last CUDA error (draft_head_last_cuda_error)
 // and return DH_ERR_CUDA.
 int record_cuda_error(cudaError_t e);

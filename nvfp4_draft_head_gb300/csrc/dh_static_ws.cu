@@ -46,48 +46,20 @@ int static_scratch(void** out) {
 
 extern "C" int draft_head_top_tokens_static(const dh_head_t* hd, const void* h, int M, int32_t* ids,
                                             float* top_logit, void* stream) {
-    if (hd == nullptr || h == nullptr || ids == nullptr) return DH_ERR_ARG;
-    if (M < 1 || M > DH_MAX_M) return DH_ERR_SHAPE;  // the scratch holds slots for 16 drafts
-    if (hd->q == nullptr) return DH_ERR_ARG;
-    if (hd->fmt != DH_FMT_NVFP4 && hd->fmt != DH_FMT_FP8 && hd->fmt != DH_FMT_BF16 && hd->fmt != DH_FMT_NVFP4_PACKED &&
-        hd->fmt != DH_FMT_FP8_W8A8)
-        return DH_ERR_ARG;
-    if (hd->V <= 0 || hd->N <= 0 || hd->n_kept < 1 || hd->n_kept > hd->N || hd->N % 64 != 0)
-        return DH_ERR_SHAPE;
-    if (!dh::gemv_supported(hd->fmt, hd->K)) return DH_ERR_SHAPE;
-    if (hd->fmt == DH_FMT_NVFP4 && (hd->sf == nullptr || hd->scale == nullptr)) return DH_ERR_ARG;
-    if ((hd->fmt == DH_FMT_FP8 || hd->fmt == DH_FMT_NVFP4_PACKED || hd->fmt == DH_FMT_FP8_W8A8) &&
-        hd->scale == nullptr)
-        return DH_ERR_ARG;
-    if (hd->idx == nullptr && (hd->fmt != DH_FMT_BF16 || hd->n_kept != hd->N || hd->N > hd->V))
-        return DH_ERR_ARG;
-    const uintptr_t al16 = reinterpret_cast<uintptr_t>(hd->q) | reinterpret_cast<uintptr_t>(h) |
-                           reinterpret_cast<uintptr_t>(hd->sf);
-    if ((al16 & 15u) != 0 || (reinterpret_cast<uintptr_t>(ids) & 3u) != 0 ||
-        (reinterpret_cast<uintptr_t>(top_logit) & 3u) != 0)
+    int st = dh::check_step_args(hd, h, M);  // M <= 16: the scratch holds slots for 16 drafts
+    if (st != DH_OK) return st;
+    if (ids == nullptr) return DH_ERR_ARG;
+    if ((reinterpret_cast<uintptr_t>(ids) & 3u) != 0 || (reinterpret_cast<uintptr_t>(top_logit) & 3u) != 0)
         return DH_ERR_ALIGN;
 
     void* scratch = nullptr;
-    int st = static_scratch(&scratch);
+    st = static_scratch(&scratch);
     if (st != DH_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
 
-    dh::GemvArgs a{};
-    a.fmt = hd->fmt;
-    a.K = hd->K;
-    a.V = hd->V;
-    a.N = hd->N;
-    a.n_kept = hd->n_kept;
-    a.q = hd->q;
-    a.sf = hd->sf;
-    a.scale = hd->scale;
-    a.idx = hd->idx;
-    a.idx_ascending = (hd->idx == nullptr || (hd->flags & DH_HEAD_IDX_ASCENDING)) ? 1 : 0;
-    a.h = static_cast<const uint16_t*>(h);
-    a.M = M;
+    dh::GemvArgs a = dh::step_args(hd, h, M, scratch);
     a.ids = ids;
     a.top = top_logit;
-    a.ws = static_cast<dh::Workspace*>(scratch);
     const cudaError_t e = dh::launch_gemv(a, s);
     return e == cudaSuccess ? DH_OK : dh::record_cuda_error(e);
 }

@@ -122,6 +122,17 @@ def test_top_tokens_rejects_bad_arguments(L, kw, M, status):
     d = _desc(**kw)
     st = L.draft_head_top_tokens(C.byref(d), H, M, 0x300000, None, WS, 256, None)
     assert st == status
+    # the static-scratch entry point applies the same checks before any CUDA call
+    assert L.draft_head_top_tokens_static(C.byref(d), H, M, 0x300000, None, None) == status
+
+
+def test_static_entry_point_pointer_checks(L):
+    d = _desc()
+    assert L.draft_head_top_tokens_static(C.byref(d), H, 1, None, None, None) == dh.DH_ERR_ARG
+    assert L.draft_head_top_tokens_static(C.byref(d), H, 1, 0x300002, None, None) == dh.DH_ERR_ALIGN
+    assert L.draft_head_top_tokens_static(C.byref(d), H, 1, 0x300000, 0x400001, None) == dh.DH_ERR_ALIGN
+    assert L.draft_head_top_tokens_static(C.byref(d), H + 8, 1, 0x300000, None, None) == dh.DH_ERR_ALIGN
+    assert L.draft_head_top_tokens_static(None, H, 1, 0x300000, None, None) == dh.DH_ERR_ARG
 
 
 def test_workspace_and_pointer_checks(L):
