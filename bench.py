@@ -318,24 +318,19 @@ def run_ours(args, world, rank, local):
         torch.distributed.barrier()
     assert head.device_error() == 0
 
-    # End to end through the public call with host buffers: per step, copy the
-    # hidden state from pinned host memory, run the draft step, read the id back.
+    # End to end through the public call with host buffers
+    # (draft_head_top_tokens_host): per step, one call copies the hidden state
+    # from pinned host memory, runs the draft step and copies the id back.
     h_pin = torch.from_numpy(hs_host.view(np.int16)).view(torch.bfloat16).pin_memory()
     ids_pin = torch.empty((Wm + K, 1), dtype=torch.int32).pin_memory()
-    h_dev = torch.empty((1, K_HID), dtype=torch.bfloat16, device=dev)
-    id_dev = torch.empty(1, dtype=torch.int32, device=dev)
     with torch.cuda.stream(s):
         for i in range(Wm):
-            h_dev.copy_(h_pin[i:i + 1], non_blocking=True)
-            heads[i % COPIES].top_tokens(h_dev, ids=id_dev)
-            ids_pin[i].copy_(id_dev, non_blocking=True)
+            heads[i % COPIES].top_tokens_host(h_pin[i:i + 1], ids_pin[i])
         torch.cuda.synchronize()
         f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         f0.record(s)
         for i in range(Wm, Wm + K):
-            h_dev.copy_(h_pin[i:i + 1], non_blocking=True)
-            heads[i % COPIES].top_tokens(h_dev, ids=id_dev)
-            ids_pin[i].copy_(id_dev, non_blocking=True)
+            heads[i % COPIES].top_tokens_host(h_pin[i:i + 1], ids_pin[i])
         f1.record(s)
         torch.cuda.synchronize()
         ms_e2e = f0.elapsed_time(f1)
@@ -403,7 +398,7 @@ def run_ours(args, world, rank, local):
                        "bytes_per_launch": STEP_BYTES},
           "cpu_baseline": cpu, "cpu_baseline_all_cores": cpu_all,
           "e2e": {"value": whole_job_us_per_step(ms_e2e, K, world), "unit": "us/step", "h2d_bytes_per_step": 2 * K_HID,
-                  "d2h_bytes_per_step": 4, "ids_match_graph": e2e_ok},
+                  "d2h_bytes_per_step": 4, "ids_match_graph": e2e_ok, "call": "draft_head_top_tokens_host"},
           "gpu_launches": K, "clocks": clocks, "parity": parity,
           "library": os.path.relpath(dh.library_path(), ROOT), "kernel_sha": sha})
     if world > 1:

@@ -181,7 +181,11 @@ int fp8_quantize_activations(const void *h, int M, int K, uint8_t *qx, float *sx
  *   K % 128 == 0. One kernel on `stream`. A pure byte permutation. */
 int nvfp4_pack_head(const uint8_t *q, const uint8_t *sf, int N, int K, uint8_t *packed, void *stream);
 
-/* Bytes of workspace the draft-step calls need for up to M_max drafts. */
+/* Bytes of workspace the draft-step calls need for up to M_max drafts (a
+ * multiple of DH_WORKSPACE_ALIGN). With a head descriptor (hd not NULL,
+ * hd->K > 0) the size includes the staging area of draft_head_top_tokens_host
+ * for min(M_max, 16) hidden rows of that K; with hd NULL it is the draft-step
+ * part alone. */
 size_t draft_head_workspace_bytes(const dh_head_t *hd, int M_max);
 
 /* Zero a draft-step workspace (error word, per-CTA argmax slots). Call once
@@ -198,6 +202,23 @@ int draft_head_workspace_init(void *ws, size_t ws_bytes, void *stream);
  * One kernel launch; capturable in a CUDA graph (no allocation, no sync). */
 int draft_head_top_tokens(const dh_head_t *hd, const void *h, int M, int32_t *ids,
                           float *top_logit, void *ws, size_t ws_bytes, void *stream);
+
+/* get_top_tokens for a caller whose hidden states and ids live in host
+ * memory (the drafter's loop on the CPU side of a serving process). One call
+ * enqueues on `stream`: the copy of h_host (BF16 [M][K] row-major, any
+ * alignment) into the staging area at the end of ws, the draft step of
+ * draft_head_top_tokens on it, and the copies of the ids (int32 [M]) and,
+ * when top_host is not NULL, the top logits (fp32 [M]) back to ids_host /
+ * top_host. It returns once they are enqueued; the host results are valid
+ * after the stream synchronises. Page-locked host buffers keep the copies
+ * asynchronous (pageable ones work, but the copies then wait on the calling
+ * thread, and stream capture refuses them). The caller owns every buffer;
+ * ws must be draft_head_workspace_bytes(hd, M_max) bytes with M_max >= M and
+ * initialised; calls that overlap on the GPU must not share a workspace.
+ * Errors: as draft_head_top_tokens (no alignment rule on the host buffers),
+ * DH_ERR_WORKSPACE when ws has no room for M staged rows of this K. */
+int draft_head_top_tokens_host(const dh_head_t *hd, const void *h_host, int M, int32_t *ids_host,
+                               float *top_host, void *ws, size_t ws_bytes, void *stream);
 
 /* compute_logits ("q38_draft.py" compute_logits; "FP8 MTP draft stack ...",
  * Qwen3_5MTP.compute_logits): out fp32 [M][V] row-major, 16-byte aligned;
@@ -230,7 +251,7 @@ int nvfp4_linear(const dh_head_t *w, const void *x, int M, float *y, void *ws, s
  * Same arguments and results as draft_head_top_tokens, minus the workspace.
  * Its scratch is one fixed array inside the library, laid out as a
  * draft-step workspace (argmax slots for at most DH_MAX_M = 16 drafts, an
- * error word; draft_head_workspace_bytes() bytes); every GPU that loads the
+ * error word; draft_head_workspace_bytes(NULL, 16) bytes); every GPU that loads the
  * library holds it until the process exits. M > 16 returns DH_ERR_SHAPE.
  * The first call on a device looks up the array's device address
  * (cudaGetSymbolAddress) with that device current; make that first call

@@ -37,7 +37,7 @@ EXPORTS = (
     "draft_head_top_tokens", "draft_head_compute_logits", "draft_head_read_device_error",
     "draft_head_status_string", "draft_head_abi_version", "draft_head_top_tokens_static",
     "nvfp4_pack_head", "fp8_quantize_activations", "draft_head_last_cuda_error", "nvfp4_linear",
-    "draft_head_wait_probe",
+    "draft_head_wait_probe", "draft_head_top_tokens_host",
 )
 
 _lib = None
@@ -84,6 +84,7 @@ def lib():
         L.draft_head_workspace_bytes.restype = S
         L.draft_head_workspace_init.argtypes = [P, S, P]
         L.draft_head_top_tokens.argtypes = [C.POINTER(dh_head_t), P, I, P, P, P, S, P]
+        L.draft_head_top_tokens_host.argtypes = [C.POINTER(dh_head_t), P, I, P, P, P, S, P]
         L.draft_head_compute_logits.argtypes = [C.POINTER(dh_head_t), P, I, P, P, S, P]
         L.draft_head_read_device_error.argtypes = [P, P, P]
         L.draft_head_status_string.argtypes = [I]
@@ -268,6 +269,28 @@ class DraftHead:
                lib().draft_head_top_tokens(C.byref(self.desc), h.data_ptr(), M, ids.data_ptr(),
                                            _ptr(top), self.ws.data_ptr(), self.ws_bytes,
                                            _stream(stream)))
+        return ids
+
+    def top_tokens_host(self, h: torch.Tensor, ids: torch.Tensor | None = None,
+                        top: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+        """get_top_tokens on host tensors: h a CPU bfloat16 [M, K] tensor; ids
+        (returned) a CPU int32 [M] tensor; top an optional CPU float32 [M] tensor.
+        One C call enqueues the copy of h to the device, the draft step and the
+        copies back; the results are valid once the stream synchronises. Pinned
+        tensors keep the copies asynchronous."""
+        if h.device.type != "cpu":
+            raise ValueError("h must be a host (CPU) tensor")
+        M = self._check_h(h)
+        if ids is None:
+            ids = torch.empty(M, dtype=torch.int32, pin_memory=h.is_pinned())
+        for name, t, dt in (("ids", ids, torch.int32), ("top", top, torch.float32)):
+            if t is not None and (t.device.type != "cpu" or t.dtype != dt or t.numel() != M
+                                  or not t.is_contiguous()):
+                raise ValueError(f"{name} must be a contiguous CPU {dt} tensor of {M} elements")
+        _check("draft_head_top_tokens_host",
+               lib().draft_head_top_tokens_host(C.byref(self.desc), h.data_ptr(), M, ids.data_ptr(),
+                                                _ptr(top), self.ws.data_ptr(), self.ws_bytes,
+                                                _stream(stream)))
         return ids
 
     def compute_logits(self, h: torch.Tensor, out: torch.Tensor | None = None,

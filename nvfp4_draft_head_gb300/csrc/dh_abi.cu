@@ -32,6 +32,14 @@ int check_ws(const void* ws, size_t ws_bytes, size_t need) {
     return DH_OK;
 }
 
+// Staging area of draft_head_top_tokens_host, after the draft-step part of a
+// workspace: M hidden rows (BF16, K each), then M ids and M top logits.
+constexpr size_t kStageIds = 2 * DH_MAX_M * sizeof(int32_t);
+static_assert(sizeof(dh::Workspace) % DH_WORKSPACE_ALIGN == 0, "the staging area starts aligned");
+size_t round_up(size_t n, size_t a) { return (n + a - 1) / a * a; }
+size_t stage_h_bytes(int K, int M) { return round_up(static_cast<size_t>(M) * static_cast<size_t>(K) * 2, DH_WORKSPACE_ALIGN); }
+size_t stage_bytes(int K, int M) { return stage_h_bytes(K, M) + round_up(kStageIds, DH_WORKSPACE_ALIGN); }
+
 int check_gather(const void* W, int V, int K, const int32_t* idx, int N) {
     if (W == nullptr || idx == nullptr) return DH_ERR_ARG;
     if (V <= 0 || K <= 0 || N <= 0) return DH_ERR_SHAPE;
@@ -180,9 +188,9 @@ int nvfp4_pack_head(const uint8_t* q, const uint8_t* sf, int N, int K, uint8_t* 
 }
 
 size_t draft_head_workspace_bytes(const dh_head_t* hd, int M_max) {
-    (void)hd;
-    (void)M_max;
-    return sizeof(dh::Workspace);
+    size_t b = sizeof(dh::Workspace);
+    if (hd != nullptr && hd->K > 0 && M_max >= 1) b += stage_bytes(hd->K, M_max < DH_MAX_M ? M_max : DH_MAX_M);
+    return b;
 }
 
 int draft_head_workspace_init(void* ws, size_t ws_bytes, void* stream) {
@@ -202,6 +210,28 @@ int draft_head_top_tokens(const dh_head_t* hd, const void* h, int M, int32_t* id
     a.ids = ids;
     a.top = top_logit;
     return cuda_status(dh::launch_gemv(a, static_cast<cudaStream_t>(stream)));
+}
+
+int draft_head_top_tokens_host(const dh_head_t* hd, const void* h_host, int M, int32_t* ids_host, float* top_host,
+                               void* ws, size_t ws_bytes, void* stream) {
+    int st = check_head(hd);
+    if (st != DH_OK) return st;
+    if (h_host == nullptr || ids_host == nullptr) return DH_ERR_ARG;
+    if (M < 1 || M > DH_MAX_M) return DH_ERR_SHAPE;
+    if ((st = check_ws(ws, ws_bytes, sizeof(dh::Workspace) + stage_bytes(hd->K, M))) != DH_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint8_t* stage = static_cast<uint8_t*>(ws) + sizeof(dh::Workspace);
+    int32_t* ids = reinterpret_cast<int32_t*>(stage + stage_h_bytes(hd->K, M));
+    float* top = reinterpret_cast<float*>(ids + DH_MAX_M);
+    cudaError_t e = cudaMemcpyAsync(stage, h_host, static_cast<size_t>(M) * hd->K * 2, cudaMemcpyHostToDevice, s);
+    if (e != cudaSuccess) return cuda_status(e);
+    dh::GemvArgs a = dh::step_args(hd, stage, M, ws);
+    a.ids = ids;
+    a.top = top_host ? top : nullptr;
+    if ((e = dh::launch_gemv(a, s)) != cudaSuccess) return cuda_status(e);
+    e = cudaMemcpyAsync(ids_host, ids, M * sizeof(int32_t), cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess && top_host) e = cudaMemcpyAsync(top_host, top, M * sizeof(float), cudaMemcpyDeviceToHost, s);
+    return cuda_status(e);
 }
 
 int draft_head_compute_logits(const dh_head_t* hd, const void* h, int M, float* out, void* ws,

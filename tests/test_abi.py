@@ -122,8 +122,29 @@ def test_top_tokens_rejects_bad_arguments(L, kw, M, status):
     d = _desc(**kw)
     st = L.draft_head_top_tokens(C.byref(d), H, M, 0x300000, None, WS, 256, None)
     assert st == status
-    # the static-scratch entry point applies the same checks before any CUDA call
+    # the static-scratch and host-buffer entry points apply the same checks before any CUDA call
     assert L.draft_head_top_tokens_static(C.byref(d), H, M, 0x300000, None, None) == status
+    assert L.draft_head_top_tokens_host(C.byref(d), H, M, 0x300000, None, WS, 1 << 30, None) == status
+
+
+def test_host_entry_point_checks(L):
+    d = _desc()
+    need = L.draft_head_workspace_bytes(C.byref(d), 4)
+    # staging for 4 rows of K = 256 BF16 values (2 KB) and the ids / top logits
+    assert need == L.draft_head_workspace_bytes(None, 16) + 2048 + 256
+    assert L.draft_head_workspace_bytes(C.byref(d), 16) == L.draft_head_workspace_bytes(None, 16) + 8192 + 256
+    assert L.draft_head_workspace_bytes(C.byref(d), 64) == L.draft_head_workspace_bytes(C.byref(d), 16)
+    assert L.draft_head_top_tokens_host(C.byref(d), None, 4, 0x300000, None, WS, need, None) == dh.DH_ERR_ARG
+    assert L.draft_head_top_tokens_host(C.byref(d), H, 4, None, None, WS, need, None) == dh.DH_ERR_ARG
+    assert L.draft_head_top_tokens_host(None, H, 4, 0x300000, None, WS, need, None) == dh.DH_ERR_ARG
+    assert L.draft_head_top_tokens_host(C.byref(d), H, 4, 0x300000, None, None, need, None) == dh.DH_ERR_ARG
+    assert L.draft_head_top_tokens_host(C.byref(d), H, 4, 0x300000, None, WS + 16, need, None) == dh.DH_ERR_WORKSPACE
+    # host buffers carry no alignment rule: a workspace one byte short is the first error
+    assert L.draft_head_top_tokens_host(C.byref(d), H + 2, 4, 0x300001, 0x400003, WS, need - 1,
+                                        None) == dh.DH_ERR_WORKSPACE
+    # the draft-step part alone has no room for the staging area
+    assert L.draft_head_top_tokens_host(C.byref(d), H, 1, 0x300000, None, WS,
+                                        L.draft_head_workspace_bytes(None, 16), None) == dh.DH_ERR_WORKSPACE
 
 
 def test_static_entry_point_pointer_checks(L):

@@ -1,6 +1,7 @@
 """Parity at the pages' full sizes (V = 248,320, K = 2560), GPU vs oracle:
   * the 64,064-row NVFP4 head: gather + quantise bit-exact, draft steps at
-    M = 1 (fresh hidden states, the launch configuration the benchmark times);
+    M = 1 (fresh hidden states, the launch configuration the benchmark times),
+    and through the host-buffer entry point;
   * the batch sweep M in {1, 2, 4, 8, 16} with planted near-ties (top-2 oracle
     gap < 1e-3 in 5 % of rows), both get_top_tokens and compute_logits;
   * the 98,304-row FP8 head: quantise bit-exact, M = 1 and 4, both paths,
@@ -81,6 +82,28 @@ def test_qwen64k_m1_steps(qwen64k, head64k, canon64k):
         if step < 2:
             run_step(canon64k, h, oracle.FMT_NVFP4, q_o, sf_o, g_o, qwen64k.idx, qwen64k.n_kept, qwen64k.V,
                      f"qwen64k canonical M=1 step {step}")
+
+
+def test_qwen64k_host_buffer_entry_point(qwen64k, head64k):
+    """draft_head_top_tokens_host on the benchmark's head, from one to sixteen
+    drafts: ids equal the device entry point's; M = 1 and 5 are also checked
+    against the oracle."""
+    q_o, sf_o, g_o = qwen64k.nvfp4()
+    for M in (1, 4, 5, 16):
+        hb = syn.hidden_bf16(syn.hidden_seed(4, M), M, qwen64k.K)
+        h_pin = torch.from_numpy(hb.view(np.int16)).view(torch.bfloat16).pin_memory()
+        top = torch.empty(M, dtype=torch.float32).pin_memory()
+        ids = head64k.top_tokens_host(h_pin, top=top)
+        torch.cuda.synchronize()
+        ids = ids.numpy()
+        assert np.array_equal(ids, head64k.top_tokens(dev_bf16(hb)).cpu().numpy()), M
+        if M in (1, 5):
+            y, A = oracle.gemv(oracle.FMT_NVFP4, q_o, sf_o, g_o, hb)
+            rows = ids_to_rows(ids, qwen64k.idx, qwen64k.n_kept)
+            check_argmax_rows(rows, y, A, qwen64k.n_kept, f"host entry qwen64k M={M}")
+            check_logits(top.numpy()[:, None], y[np.arange(M), rows][:, None], A[np.arange(M), rows][:, None],
+                         f"host entry qwen64k M={M} top logit")
+    assert head64k.device_error() == 0
 
 
 @pytest.mark.parametrize("M", [1, 2, 4, 8, 16])

@@ -417,6 +417,70 @@ def test_cuda_graph_replay(tiny):
         assert np.array_equal(ids, eager)
 
 
+@pytest.mark.parametrize("pinned", [True, False])
+def test_host_buffer_entry_point(tiny, pinned):
+    """draft_head_top_tokens_host: hidden rows and ids in host memory, one call
+    per step. Several steps are enqueued back to back (each reuses the staging
+    area after the previous step's draft step, in stream order) before one
+    synchronise; ids equal the device entry point's and meet the oracle."""
+    head, _ = gpu_nvfp4(tiny, packed=True)
+    q_o, sf_o, g_o = tiny.nvfp4()
+    steps = [(M, syn.hidden_bf16(syn.hidden_seed(0, 9500 + i), M, tiny.K)) for i, M in enumerate((1, 5, 16, 2))]
+    outs = []
+    for M, hb in steps:
+        h = torch.from_numpy(hb.view(np.int16)).view(torch.bfloat16)
+        h = h.pin_memory() if pinned else h
+        ids = torch.full((M,), -7, dtype=torch.int32, pin_memory=pinned)
+        top = torch.full((M,), np.nan, dtype=torch.float32, pin_memory=pinned)
+        outs.append((head.top_tokens_host(h, ids, top), top))
+    torch.cuda.synchronize()
+    assert head.device_error() == 0
+    for (M, hb), (ids, top) in zip(steps, outs):
+        ids = ids.numpy()
+        assert np.array_equal(ids, head.top_tokens(dev_bf16(hb)).cpu().numpy())
+        y, A = oracle.gemv(oracle.FMT_NVFP4, q_o, sf_o, g_o, hb)
+        rows = ids_to_rows(ids, tiny.idx, tiny.n_kept)
+        check_argmax_rows(rows, y, A, tiny.n_kept, f"host entry M={M}")
+        check_logits(top.numpy()[:, None], y[np.arange(M), rows][:, None], A[np.arange(M), rows][:, None],
+                     f"host entry M={M} top logit")
+    # the W8A8 head through the same entry point
+    W = dev_bf16(tiny.W)
+    h8 = dh.fp8_head(W, tiny.keep, w8a8=True)
+    hb = syn.hidden_bf16(syn.hidden_seed(0, 9600), 3, tiny.K)
+    ids = h8.top_tokens_host(torch.from_numpy(hb.view(np.int16)).view(torch.bfloat16))
+    torch.cuda.synchronize()
+    assert np.array_equal(ids.numpy(), h8.top_tokens(dev_bf16(hb)).cpu().numpy())
+    with pytest.raises(ValueError):
+        head.top_tokens_host(dev_bf16(hb))                 # a device tensor is refused
+
+
+def test_host_buffer_entry_point_in_a_cuda_graph(tiny):
+    """Under stream capture the host-buffer entry point copies h_host in stream
+    order, so every replay reads the pinned buffer's current contents."""
+    head, _ = gpu_nvfp4(tiny, packed=True)
+    q_o, sf_o, g_o = tiny.nvfp4()
+    M = 3
+    h_pin = torch.zeros((M, tiny.K), dtype=torch.bfloat16).pin_memory()
+    ids_pin = torch.full((M,), -7, dtype=torch.int32).pin_memory()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        head.top_tokens_host(h_pin, ids_pin)                 # warm-up outside capture
+    s.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        head.top_tokens_host(h_pin, ids_pin, stream=s)
+    for step in range(3):
+        hb = syn.hidden_bf16(syn.hidden_seed(0, 9700 + step), M, tiny.K)
+        h_pin.copy_(torch.from_numpy(hb.view(np.int16)).view(torch.bfloat16))
+        graph.replay()
+        torch.cuda.synchronize()
+        ids = ids_pin.numpy().copy()
+        assert np.array_equal(ids, head.top_tokens(dev_bf16(hb)).cpu().numpy()), step
+        y, A = oracle.gemv(oracle.FMT_NVFP4, q_o, sf_o, g_o, hb)
+        check_argmax_rows(ids_to_rows(ids, tiny.idx, tiny.n_kept), y, A, tiny.n_kept, f"host graph {step}")
+
+
 @pytest.mark.parametrize("kind", [0, 1])
 def test_bounded_waits_give_up_and_report(tiny, kind):
     """A wait for an event that never happens (a workspace word nothing writes;
