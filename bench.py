@@ -353,7 +353,8 @@ def run_ours(args, world, rank, local):
         nwin = 2 * Kh // 128
         packed_o = np.concatenate(
             [q_o.reshape(N_ // 16, 16, nwin, 64).transpose(0, 2, 1, 3).reshape(N_ // 16, nwin, 1024),
-             sf_o.reshape(N_ // 16, 16, nwin, 8).transpose(0, 2, 1, 3).reshape(N_ // 16, nwin, 128)], axis=2)
+             sf_o.reshape(N_ // 16, 2, 8, nwin, 4, 2).transpose(0, 3, 2, 4, 1, 5).reshape(N_ // 16, nwin, 128)],
+            axis=2)
         exact = (np.array_equal(head.q.cpu().numpy(), packed_o) and head.scale.cpu().numpy()[0] == g_o)
         n_chk = min(3, K)
         got = ids[Wm:Wm + n_chk, 0].cpu().numpy()

@@ -175,7 +175,9 @@ int fp8_quantize_activations(const void *h, int M, int K, uint8_t *qx, float *sx
  * row-major one ("q38_draft.py": NVFP4Linear(W, "marlin")). For each tile of
  * 16 rows and each 128-wide k-window w (in that order), `packed` holds a
  * 1,152-byte block: the 16 rows' code bytes 64w..64w+63 (row by row), then
- * their scale bytes 8w..8w+7 (row by row).
+ * 128 bytes of their scales 8w..8w+7: for g < 8 and t < 4, bytes
+ * 4 (4 g + t) .. 4 (4 g + t) + 3 hold the scales of blocks 8w + 2t and
+ * 8w + 2t + 1 of tile row g, then the same two of tile row g + 8.
  *   q [N][K/2], sf [N][K/16] as written by nvfp4_quantize_rows; packed: device
  *   buffer of N * (K/2 + K/16) bytes. All three 16-byte aligned; N % 16 == 0,
  *   K % 128 == 0. One kernel on `stream`. A pure byte permutation. */

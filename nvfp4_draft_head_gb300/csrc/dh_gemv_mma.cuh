@@ -24,12 +24,13 @@
 // NVFP4 with one draft (the headline case) uses a block-diagonal B: the 8
 // columns of the MMA are the 8 E4M3 blocks of a window instead of 8 drafts.
 // Slot pair p of the 16 k-slots carries elements (2i, 2i+1) of block pi(p) in
-// MMA i (i < 8), and B[slot][col] is h there when col == p and 0 otherwise, so
-// after the 8 MMAs of a window D[row][col] is the un-scaled sum of block pi(col)
-// of that row. Each thread then applies the two E4M3 scales of its two D
-// columns with 4 FFMAs per window instead of one per weight.
-// pi(p) = 2p for p < 4, 2(p-4)+1 for p >= 4 makes thread t's blocks 2t, 2t+1,
-// i.e. its 32 consecutive codes.
+// MMA i (i < 8), and B[slot][col] is h there when col == pi(p) and 0
+// otherwise, so after the 8 MMAs of a window D[row][col] is the un-scaled sum
+// of block col of that row. Each thread then applies the two E4M3 scales of
+// its two D columns 2t, 2t+1 with 4 FFMAs per window instead of one per weight.
+// pi(p) = 2p for p < 4, 2(p-4)+1 for p >= 4 makes thread t's A slots hold
+// blocks 2t, 2t+1, i.e. its 32 consecutive codes, and its D columns the same
+// two blocks, whose scales it loads as one word in the packed layout.
 // With several drafts (and for FP8 / BF16) the 8 columns are drafts: the NVFP4
 // codes are multiplied by their block scale in f16 first (exact: at most 6
 // significant bits, magnitude at most 2688), and D accumulates over all k.
@@ -97,7 +98,9 @@ struct Cfg {
     static constexpr int CPR = WB / 4 / 16;                   // 16-byte loads per row, window, thread
     static constexpr int SFB = NV ? K / 16 : 0;               // scale bytes per head row
     static constexpr int WBLK = 16 * WB + 16 * 8;             // packed: bytes of one (tile, window) block
-    static constexpr int TILE_REGS = WPW * (8 * CPR + (NV ? 4 : 0));
+    // registers of one tile's loads: the codes, plus (NVFP4) the scale bytes:
+    // one word in the packed layout, two rows' 8 bytes in the canonical one
+    static constexpr int TILE_REGS = WPW * (8 * CPR + (PACKED ? 1 : (NV ? 4 : 0)));
     // NVFP4 at 4 and 8 drafts: the B fragments (h) come from shared memory (one
     // 8-byte load per MMA) instead of 16 registers: 22.1 -> 21.9 and 24.6 -> 23.7
     // µs per step. Slower at 2 drafts (+0.5 µs) and at 16 (+2.3 µs with two
@@ -106,9 +109,15 @@ struct Cfg {
     static constexpr bool SMB = PACKED && !BLOCKDIAG && WPW == 1 && (MT == 4 || MT == 8);
     // tiles of loads in flight in registers: as many as fit, next to the h
     // fragments (16 registers per window and n8 tile), in the 80 registers that
-    // 21+ warps per SM allow: three with one window per warp and one n8 tile,
-    // two at 16 drafts, one with two windows per warp (K = 4096, 5120)
-    static constexpr int P = SMB ? 3 : cmax(1, cmin(MT >= 16 ? 2 : 3, (kLoadRegBudget - WPW * NT * 16) / TILE_REGS));
+    // 21+ warps per SM allow, up to a cap: three with one window per warp and
+    // one n8 tile, two at 16 drafts, one with two windows per warp (K = 4096,
+    // 5120). The packed NVFP4 head (9 registers a tile) measured best with two
+    // at one draft (20.00 -> 19.94 µs top tokens, 22.14 -> 21.76 compute_logits
+    // against three), four at two and eight drafts (21.43 -> 20.99, 22.19 ->
+    // 21.55 against three; four at four drafts was slower) and two at 16
+    // (three spilled: 27.5 -> 33.4).
+    static constexpr int PCAP = PACKED ? (MT == 1 ? 2 : (MT == 2 ? 4 : (MT >= 16 ? 2 : 3))) : (MT >= 16 ? 2 : 3);
+    static constexpr int P = SMB ? (MT == 8 ? 4 : 3) : cmax(1, cmin(PCAP, (kLoadRegBudget - WPW * NT * 16) / TILE_REGS));
     // Canonical NVFP4 layout: a loader warp streams each tile's scale bytes
     // into a shared-memory ring with 1-D bulk copies.
     static constexpr bool SCALES = (FMT == 1);
@@ -156,14 +165,16 @@ __device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
 }
 
 // Code bytes of one tile held by one thread: per window, CPR 16-byte pieces of
-// row g and of row g+8, and for NVFP4 the window's 8 scale bytes of both rows
-// (loaded with the codes from the packed layout, or taken from the shared-
-// memory scale ring for the canonical layout).
+// row g and of row g+8, and for NVFP4 the scale bytes: in the packed layout the
+// word with the scales of blocks 2t, 2t+1 of rows g and g+8 (loaded with the
+// codes), in the canonical one the window's 8 scale bytes of both rows (taken
+// from the shared-memory scale ring).
 template <int FMT, int K, int MT>
 struct TileBuf {
     using C = Cfg<FMT, K, MT>;
     uint4 c[C::WPW][2][C::CPR];
     uint2 s[C::WPW][2];
+    uint32_t sp[C::WPW];
 };
 
 template <int FMT, int K, int MT>
@@ -174,16 +185,12 @@ __device__ __forceinline__ void load_tile(TileBuf<FMT, K, MT>& b, const uint8_t*
     for (int ww = 0; ww < C::WPW; ++ww) {
         const int w = warp + ww * C::NW;
         if constexpr (C::PACKED) {
-            // block (tile, w): 16 rows x 64 code bytes, then 16 rows x 8 scale bytes
+            // block (tile, w): 16 rows x 64 code bytes, then 4 scale bytes per lane
             const uint8_t* blk = q + (static_cast<size_t>(tile) * C::NWIN + w) * C::WBLK;
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                b.c[ww][h][0] = ld_stream_v4(blk + (g + 8 * h) * 64 + 16 * t);
-                uint2 v;
-                asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];"
-                             : "=r"(v.x), "=r"(v.y) : "l"(blk + 16 * 64 + (g + 8 * h) * 8));
-                b.s[ww][h] = v;
-            }
+            for (int h = 0; h < 2; ++h) b.c[ww][h][0] = ld_stream_v4(blk + (g + 8 * h) * 64 + 16 * t);
+            asm volatile("ld.global.nc.L1::no_allocate.u32 %0, [%1];"
+                         : "=r"(b.sp[ww]) : "l"(blk + 16 * 64 + 4 * (4 * g + t)));
         } else {
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
@@ -539,9 +546,10 @@ __global__ void __launch_bounds__(Cfg<FMT, K, MT>::THREADS, 1) gemv_mma_kernel(c
                 for (int ww = 0; ww < WPW; ++ww)
 #pragma unroll
                     for (int j = 0; j < 16; ++j) {
-                        // b0 of MMA i is nonzero only for t == g (pair p = t), b1 only
-                        // for t + 4 == g (pair p = t + 4)
-                        const bool keep = (j < 8) ? (t == g) : (t + 4 == g);
+                        // slot pair p (block pi(p)) feeds D column pi(p): b0 of MMA i
+                        // (pair t, block 2t) is nonzero only in column g == 2t, b1 (pair
+                        // t + 4, block 2t + 1) only in column g == 2t + 1
+                        const bool keep = (j < 8) ? (g == 2 * t) : (g == 2 * t + 1);
                         hb[ww][nt][j] = keep ? hb[ww][nt][j] : 0u;
                     }
             } else {
@@ -559,10 +567,6 @@ __global__ void __launch_bounds__(Cfg<FMT, K, MT>::THREADS, 1) gemv_mma_kernel(c
                 for (int i = 0; i < 8; ++i) s_hb[(nt * 8 + i) * 32 + lane] = make_uint2(hb[0][nt][2 * i], hb[0][nt][2 * i + 1]);
             __syncwarp();
         }
-        // Blocks of this thread's D columns 2t, 2t+1 under pi (block-diagonal case).
-        const int blk0 = (2 * t < 4) ? 4 * t : 4 * t - 7;
-        const int blk1 = blk0 + 2;
-
         for (int it = 0; it < my_tiles; it += P) {
 #pragma unroll
             for (int p = 0; p < P; ++p) {
@@ -611,11 +615,16 @@ __global__ void __launch_bounds__(Cfg<FMT, K, MT>::THREADS, 1) gemv_mma_kernel(c
                             }
                         }
 
-                        // scales of blocks blk0, blk1 of rows g, g+8 (bytes of the window's 8)
-                        const uint32_t sel = static_cast<uint32_t>(blk0) | (static_cast<uint32_t>(blk1) << 4);
+                        // scales of blocks 2t, 2t+1 (this thread's D columns) of rows g, g+8
                         uint32_t s01g, s01h;
-                        asm("prmt.b32 %0, %1, %2, %3;" : "=r"(s01g) : "r"(b.s[ww][0].x), "r"(b.s[ww][0].y), "r"(sel));
-                        asm("prmt.b32 %0, %1, %2, %3;" : "=r"(s01h) : "r"(b.s[ww][1].x), "r"(b.s[ww][1].y), "r"(sel));
+                        if constexpr (C::PACKED) {
+                            s01g = b.sp[ww];
+                            s01h = b.sp[ww] >> 16;
+                        } else {
+                            const uint32_t sel = static_cast<uint32_t>(2 * t) | (static_cast<uint32_t>(2 * t + 1) << 4);
+                            asm("prmt.b32 %0, %1, %2, %3;" : "=r"(s01g) : "r"(b.s[ww][0].x), "r"(b.s[ww][0].y), "r"(sel));
+                            asm("prmt.b32 %0, %1, %2, %3;" : "=r"(s01h) : "r"(b.s[ww][1].x), "r"(b.s[ww][1].y), "r"(sel));
+                        }
                         const uint32_t fg = e4m3x2_to_f16x2(s01g), fh = e4m3x2_to_f16x2(s01h);
                         y0 = fmaf(d[0], f16lo(fg), y0);
                         y0 = fmaf(d[1], f16hi(fg), y0);
@@ -654,10 +663,15 @@ __global__ void __launch_bounds__(Cfg<FMT, K, MT>::THREADS, 1) gemv_mma_kernel(c
                         uint32_t sg0 = 0u, sg1 = 0u, sh0 = 0u, sh1 = 0u;  // (s, s) f16x2 per row and block
                         if constexpr (C::NV) {
                             // blocks 2t, 2t+1 of the window: bytes 2t, 2t+1 of its 8 scale bytes
-                            const uint32_t sel = static_cast<uint32_t>(2 * t) | (static_cast<uint32_t>(2 * t + 1) << 4);
                             uint32_t s2g, s2h;
-                            asm("prmt.b32 %0, %1, %2, %3;" : "=r"(s2g) : "r"(b.s[ww][0].x), "r"(b.s[ww][0].y), "r"(sel));
-                            asm("prmt.b32 %0, %1, %2, %3;" : "=r"(s2h) : "r"(b.s[ww][1].x), "r"(b.s[ww][1].y), "r"(sel));
+                            if constexpr (C::PACKED) {
+                                s2g = b.sp[ww];
+                                s2h = b.sp[ww] >> 16;
+                            } else {
+                                const uint32_t sel = static_cast<uint32_t>(2 * t) | (static_cast<uint32_t>(2 * t + 1) << 4);
+                                asm("prmt.b32 %0, %1, %2, %3;" : "=r"(s2g) : "r"(b.s[ww][0].x), "r"(b.s[ww][0].y), "r"(sel));
+                                asm("prmt.b32 %0, %1, %2, %3;" : "=r"(s2h) : "r"(b.s[ww][1].x), "r"(b.s[ww][1].y), "r"(sel));
+                            }
                             const uint32_t fg = e4m3x2_to_f16x2(s2g), fh = e4m3x2_to_f16x2(s2h);
                             asm("prmt.b32 %0, %1, 0, 0x1010;" : "=r"(sg0) : "r"(fg));
                             asm("prmt.b32 %0, %1, 0, 0x3232;" : "=r"(sg1) : "r"(fg));

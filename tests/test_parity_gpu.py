@@ -39,11 +39,12 @@ def tiny():
 
 def pack_reference(q, sf):
     """Tile-major layout written out with numpy: per (16-row tile, 128-k window),
-    the 16 rows' 64 code bytes, then their 8 scale bytes."""
+    the 16 rows' 64 code bytes, then their scale bytes ordered [g][t][h][e] for
+    tile row 8 h + g and window block 2 t + e (g < 8, t < 4, h < 2, e < 2)."""
     N, Kh = q.shape
     nwin = 2 * Kh // 128
     codes = q.reshape(N // 16, 16, nwin, 64).transpose(0, 2, 1, 3).reshape(N // 16, nwin, 1024)
-    scales = sf.reshape(N // 16, 16, nwin, 8).transpose(0, 2, 1, 3).reshape(N // 16, nwin, 128)
+    scales = sf.reshape(N // 16, 2, 8, nwin, 4, 2).transpose(0, 3, 2, 4, 1, 5).reshape(N // 16, nwin, 128)
     return np.concatenate([codes, scales], axis=2)
 
 
