@@ -50,7 +50,7 @@ STEP_BYTES = N_ROWS * (K_HID // 2) + N_ROWS * (K_HID // 16) + 4 + 2 * K_HID + 4
 # launches) of one launch of the M = 1 GEMV from the ncu capture summarised in
 # profiles/gemv_nvfp4_packed_m1_qwen64k.md; reported only while the kernel
 # sources still hash to kernel_sha (else null).
-TRAFFIC = {"kernel_sha": "b72bf833f46a925c", "bytes_per_launch": 94_889_856}
+TRAFFIC = {"kernel_sha": "5bb8e36621a290d6", "bytes_per_launch": 94_749_568}
 
 
 def kernel_sha() -> str:
