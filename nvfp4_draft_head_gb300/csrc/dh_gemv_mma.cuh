@@ -115,8 +115,13 @@ struct Cfg {
     // at one draft (20.00 -> 19.94 µs top tokens, 22.14 -> 21.76 compute_logits
     // against three), four at two and eight drafts (21.43 -> 20.99, 22.19 ->
     // 21.55 against three; four at four drafts was slower) and two at 16
-    // (three spilled: 27.5 -> 33.4).
-    static constexpr int PCAP = PACKED ? (MT == 1 ? 2 : (MT == 2 ? 4 : (MT >= 16 ? 2 : 3))) : (MT >= 16 ? 2 : 3);
+    // (three spilled: 27.5 -> 33.4). The FP8 heads (16 registers a tile) take
+    // two at every draft count (98,304 rows, one draft: W8A16, where three
+    // spilled, 41.65 -> 40.66 µs top tokens and 44.14 -> 42.64 compute_logits;
+    // W8A8 39.90 -> 39.18 and 42.64 -> 41.76; W8A8 top tokens at four drafts
+    // 40.78 -> 40.98, its compute_logits 44.66 -> 43.95).
+    static constexpr int PCAP = PACKED ? (MT == 1 ? 2 : (MT == 2 ? 4 : (MT >= 16 ? 2 : 3)))
+                                       : ((MT >= 16 || FMT == 2 || FMT == 5) ? 2 : 3);
     static constexpr int P = SMB ? (MT == 8 ? 4 : 3) : cmax(1, cmin(PCAP, (kLoadRegBudget - WPW * NT * 16) / TILE_REGS));
     // Canonical NVFP4 layout: a loader warp streams each tile's scale bytes
     // into a shared-memory ring with 1-D bulk copies.
