@@ -50,7 +50,7 @@ STEP_BYTES = N_ROWS * (K_HID // 2) + N_ROWS * (K_HID // 16) + 4 + 2 * K_HID + 4
 # launches) of one launch of the M = 1 GEMV from the ncu capture summarised in
 # profiles/gemv_nvfp4_packed_m1_qwen64k.md; reported only while the kernel
 # sources still hash to kernel_sha (else null).
-TRAFFIC = {"kernel_sha": "3d0d1194cf8e4510", "bytes_per_launch": 95_090_816}
+TRAFFIC = {"kernel_sha": "94eb39504c1bb05c", "bytes_per_launch": 95_060_096}
 
 
 def kernel_sha() -> str:

@@ -133,7 +133,10 @@ struct Cfg {
     static constexpr int THREADS = (NW + NRW + (LOADER ? 1 : 0)) * 32;  // + reducers (+ loader)
     static constexpr int SLOT = 16 * SFB;                              // bytes of one ring slot
     static constexpr int SS = 6;
-    static constexpr int RS = (4 * NW * 16 * MT * 4 <= 40 * 1024) ? 4 : 2;  // partial-sum slots
+    // partial-sum slots: eight for the packed one-draft kernels (one draft 19.87 ->
+    // 19.73 µs top tokens, 21.59 -> 21.41 compute_logits against four), else four
+    // while they fit in 40 KB, else two
+    static constexpr int RS = (PACKED && MT == 1) ? 8 : ((4 * NW * 16 * MT * 4 <= 40 * 1024) ? 4 : 2);
     static_assert(NWIN % NW == 0, "windows must split evenly over warps");
     static_assert(K % 128 == 0, "K must be a multiple of 128");
 };
