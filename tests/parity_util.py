@@ -71,6 +71,18 @@ class Workload:
         return self._f8
 
 
+def pack_reference(q, sf):
+    """Tile-major layout of DH_FMT_NVFP4_PACKED written out with numpy: per
+    (16-row tile, 128-k window), the 16 rows' 64 code bytes, then their scale
+    bytes ordered [g][t][h][e] for tile row 8 h + g and window block 2 t + e
+    (g < 8, t < 4, h < 2, e < 2)."""
+    N, Kh = q.shape
+    nwin = 2 * Kh // 128
+    codes = q.reshape(N // 16, 16, nwin, 64).transpose(0, 2, 1, 3).reshape(N // 16, nwin, 1024)
+    scales = sf.reshape(N // 16, 2, 8, nwin, 4, 2).transpose(0, 3, 2, 4, 1, 5).reshape(N // 16, nwin, 128)
+    return np.concatenate([codes, scales], axis=2)
+
+
 def plant_near_ties(q, sf, g, h_bits, n_kept, frac, seed, max_tries=8):
     """Move a fraction of hidden rows so that their top-2 oracle logits (over the
     kept rows) are within 1e-3. Each try takes the current top-2 rows a, b and

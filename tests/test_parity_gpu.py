@@ -10,7 +10,8 @@ import torch
 import nvfp4_draft_head_gb300 as dh
 import oracle
 import synthetic as syn
-from parity_util import Workload, check_argmax_rows, check_logits, ids_to_rows, plant_near_ties
+from parity_util import (Workload, check_argmax_rows, check_logits, ids_to_rows, pack_reference,  # noqa: F401
+                         plant_near_ties)
 
 pytestmark = pytest.mark.gpu
 
@@ -35,17 +36,6 @@ def dev_bf16(bits):
 def tiny():
     c = syn.TINY
     return Workload(syn.SEED_HEAD_TINY, c["V"], c["K"], c["n_kept"], c["forced"], syn.SEED_KEEP_TINY)
-
-
-def pack_reference(q, sf):
-    """Tile-major layout written out with numpy: per (16-row tile, 128-k window),
-    the 16 rows' 64 code bytes, then their scale bytes ordered [g][t][h][e] for
-    tile row 8 h + g and window block 2 t + e (g < 8, t < 4, h < 2, e < 2)."""
-    N, Kh = q.shape
-    nwin = 2 * Kh // 128
-    codes = q.reshape(N // 16, 16, nwin, 64).transpose(0, 2, 1, 3).reshape(N // 16, nwin, 1024)
-    scales = sf.reshape(N // 16, 2, 8, nwin, 4, 2).transpose(0, 3, 2, 4, 1, 5).reshape(N // 16, nwin, 128)
-    return np.concatenate([codes, scales], axis=2)
 
 
 def gpu_nvfp4(wl, packed=False, ascending=None):
