@@ -47,15 +47,15 @@ N_ROWS, K_HID = 64_064, 2_560
 STEP_BYTES = N_ROWS * (K_HID // 2) + N_ROWS * (K_HID // 16) + 4 + 2 * K_HID + 4
 
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum, mean of two
-# launches) of one launch of the M = 1 GEMV from the ncu capture summarised in
-# profiles/gemv_nvfp4_packed_m1_qwen64k.md; reported only while the kernel
-# sources still hash to kernel_sha (else null).
+# launches) of one launch of the M = 1 GEMV, from an ncu capture of
+# `bench.py --profile`; reported only while the kernel sources still hash to
+# kernel_sha (else null).
 TRAFFIC = {"kernel_sha": "94eb39504c1bb05c", "bytes_per_launch": 95_060_096}
 
 
 def kernel_sha() -> str:
     h = hashlib.sha256()
-    for f in ("dh_gemv_mma.cuh", "dh_epilogue.cuh", "dh_common.cuh", "dh_gemv_nvfp4p.cu"):
+    for f in ("dh_gemv_mma.cuh", "dh_epilogue.cuh", "dh_common.cuh", "dh_gemv_nvfp4p.cu", "dh_gemv_nvfp4p_ldg.cu"):
         with open(os.path.join(ROOT, "nvfp4_draft_head_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]

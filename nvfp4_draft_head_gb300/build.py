@@ -19,7 +19,7 @@ OUT_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(OUT_DIR, "libdrafthead.so")
 
 SOURCES = ["dh_abi.cu", "dh_quantize.cu", "dh_gemv.cu", "dh_gemv_nvfp4.cu", "dh_gemv_fp8.cu",
-           "dh_gemv_bf16.cu", "dh_static_ws.cu", "dh_gemv_nvfp4p.cu", "dh_pack.cu",
+           "dh_gemv_bf16.cu", "dh_static_ws.cu", "dh_gemv_nvfp4p.cu", "dh_gemv_nvfp4p_ldg.cu", "dh_pack.cu",
            "dh_gemv_w8a8.cu", "dh_gemv_linear.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 # -fno-gnu-unique: the launchers' per-device caches (function-local statics of

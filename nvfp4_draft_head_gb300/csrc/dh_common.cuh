@@ -13,15 +13,21 @@ namespace dh {
 constexpr int kMaxGrid = 1024;
 
 // Layout of a workspace (callers allocate it). The quantisers use only the
-// 256-byte header; a draft step also uses the slots, which start at zero and
-// which the collecting CTA zeroes again after reading them.
+// 256-byte header; a draft step also uses the epoch, the dirty word and the
+// argmax slots. Draft steps alternate between two banks of slots (bank = epoch
+// & 1). The collecting CTA zeroes every slot it read and advances the epoch; a
+// slot written after its collector gave up waiting lands in a bank that the
+// next step does not use, and that step zeroes it (see the dirty word) before
+// the bank comes round again.
 struct Workspace {
     unsigned int error;      // DH_DEVERR_* bits
     unsigned int amax_bits;  // quantisers: running max |w| as float bits
-    unsigned int pad_[62];
-    // per draft and CTA: the CTA's best (ordered logit << 32 | ~id or ~row)
-    // key, or 1 when it holds no kept row; 0 while not yet published
-    unsigned long long slots[16][kMaxGrid];
+    unsigned int epoch;      // draft steps collected on this workspace
+    unsigned int dirty;      // 0, or 1 | bank << 1 | drafts << 2 | CTAs << 8 of a step whose wait ran out
+    unsigned int pad_[60];
+    // per bank, draft and CTA: the CTA's best (ordered logit << 32 | ~id or
+    // ~row) key, or 1 when it holds no kept row; 0 while not yet published
+    unsigned long long slots[2][16][kMaxGrid];
 };
 constexpr size_t kWorkspaceHeader = 256;
 static_assert(offsetof(Workspace, slots) == kWorkspaceHeader, "workspace header is 256 bytes");
@@ -199,6 +205,16 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32
         if (done) return true;
     }
     return false;
+}
+
+// Non-blocking test of the phase with the given parity: true if it completed.
+__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile("{\n\t.reg .pred p;\n\t"
+                 "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(done) : "r"(smem_u32(bar)), "r"(parity) : "memory");
+    return done != 0;
 }
 
 // Poll a 64-bit word in global memory (relaxed, device scope) until it is

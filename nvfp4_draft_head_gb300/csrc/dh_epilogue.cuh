@@ -1,6 +1,7 @@
-// Epilogues shared by the draft-step kernels: the grid-wide argmax hand-off
-// ("q38_draft.py", get_top_tokens: dh_idx[draft_head(h).argmax(-1)]) and the
-// logits scatter of compute_logits.
+// Epilogue of the draft-step kernels in top-tokens mode: the grid-wide argmax
+// ("q38_draft.py", get_top_tokens: dh_idx[draft_head(h).argmax(-1)]), or, for
+// one shard of a vocabulary-sharded head, the keys that the local-argmax
+// exchange combines ("q38_draft.py", install: use_local_argmax_reduction).
 #pragma once
 
 #include "dh_common.cuh"
@@ -8,39 +9,80 @@
 
 namespace dh {
 
+// Epoch of the workspace, read by every CTA after the grid-dependency wait
+// (the preceding step has completed, so its epoch advance is visible).
+__device__ __forceinline__ unsigned int load_epoch(const Workspace* ws) {
+    unsigned int e;
+    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(e) : "l"(&ws->epoch) : "memory");
+    return e;
+}
+
 // Grid-wide argmax hand-off. Every CTA stores its best key per draft in its
-// own workspace slot (1 when it holds no kept row). CTA 0 polls all slots
-// until each is non-zero, zeroes them for the next launch, keeps the maximum
-// and turns it into an id (the key carries the id itself when dh_idx is
-// ascending, else the row). The key is its own "published" flag, so the
-// hand-off costs one store and one poll round trip, with no fence, ticket or
-// read-back after it.
-__device__ __forceinline__ void finish_argmax(const GemvArgs& a, const unsigned long long* cta_key) {
+// own slot of bank (epoch & 1) (1 when it holds no kept row). CTA 0 polls the
+// bank's slots until each is non-zero (bounded), zeroes them, keeps the
+// maximum per draft and turns it into an id, or a shard key. The key is its
+// own "published" flag: one store and one poll round trip, no fence or ticket.
+//
+// If a poll runs out, CTA 0 records the timeout and marks the bank dirty: the
+// late CTA's store still lands there, before this launch completes. The next
+// step collects from the other bank and zeroes the dirty one, so a late key
+// never reaches a later step.
+__device__ __forceinline__ void finish_argmax(const GemvArgs& a, const unsigned long long* cta_key,
+                                              unsigned int epoch) {
+    const unsigned int bank = epoch & 1u;
     if (threadIdx.x < a.M) {
         const unsigned long long k = cta_key[threadIdx.x] != 0ull ? cta_key[threadIdx.x] : 1ull;
         asm volatile("st.relaxed.gpu.global.u64 [%0], %1;"
-                     :: "l"(&a.ws->slots[threadIdx.x][blockIdx.x]), "l"(k) : "memory");
+                     :: "l"(&a.ws->slots[bank][threadIdx.x][blockIdx.x]), "l"(k) : "memory");
     }
     if (blockIdx.x != 0) return;
     __shared__ unsigned long long s_red[16];
     __shared__ int s_late;
+    __shared__ unsigned int s_dirty;
     if (threadIdx.x < 16) s_red[threadIdx.x] = 0ull;
-    if (threadIdx.x == 0) s_late = 0;
+    if (threadIdx.x == 0) {
+        s_late = 0;
+        unsigned int d;
+        asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(d) : "l"(&a.ws->dirty) : "memory");
+        s_dirty = d;
+    }
     __syncthreads();
     const int G = static_cast<int>(gridDim.x);
     for (int j = threadIdx.x; j < G * a.M; j += blockDim.x) {
         const int m = j / G, b = j - m * G;
-        unsigned long long* p = &a.ws->slots[m][b];
+        unsigned long long* p = &a.ws->slots[bank][m][b];
         const unsigned long long v = poll_nonzero(p);
         if (v == 0ull) s_late = 1;
         asm volatile("st.relaxed.gpu.global.u64 [%0], 0;" :: "l"(p) : "memory");
         if (v > 1ull) atomicMax(&s_red[m], v);
     }
+    // a dirty bank left by an earlier step (never this step's bank): zero the
+    // slots that step used
+    if (s_dirty & 1u) {
+        const unsigned int db = (s_dirty >> 1) & 1u, dm = (s_dirty >> 2) & 31u, dg = s_dirty >> 8;
+        for (unsigned int j = threadIdx.x; j < dm * dg; j += blockDim.x)
+            asm volatile("st.relaxed.gpu.global.u64 [%0], 0;" :: "l"(&a.ws->slots[db][j / dg][j % dg]) : "memory");
+    }
     __syncthreads();
-    if (threadIdx.x == 0 && s_late) atomicOr(&a.ws->error, kDevErrTimeout);
+    if (threadIdx.x == 0) {
+        unsigned int d = 0u;
+        if (s_late) {
+            atomicOr(&a.ws->error, kDevErrTimeout);
+            d = 1u | (bank << 1) | (static_cast<unsigned int>(a.M) << 2) | (static_cast<unsigned int>(G) << 8);
+        }
+        if (s_late || (s_dirty & 1u)) a.ws->dirty = d;
+        a.ws->epoch = epoch + 1u;
+    }
     if (threadIdx.x < a.M) {
         const int m = threadIdx.x;
         const unsigned long long k = s_red[m];
+        if (a.keys) {
+            // shard key: signed order equals the unsigned order of k (an int64
+            // MAX all-reduce combines shards); a shard without a kept row gives
+            // INT64_MIN, the identity of that maximum
+            a.keys[m] = k ^ 0x8000000000000000ull;
+            return;
+        }
         // low word: 0xFFFFFFFF - id with ascending ids, else 0xFFFFFFFF - row
         const uint32_t low = 0xFFFFFFFFu - static_cast<uint32_t>(k & 0xFFFFFFFFull);
         int id = -1;

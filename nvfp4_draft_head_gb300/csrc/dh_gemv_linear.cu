@@ -13,10 +13,16 @@ bool linear_extra_k(int K) { return K == 512 || K == 1024 || K == 2048 || K == 4
 cudaError_t launch_linear_nvfp4_packed_extra(const GemvArgs& a, cudaStream_t s) {
     if (a.out == nullptr) return cudaErrorInvalidValue;
     switch (a.K) {
-        case 512: return mma::launch_mma_m<4, 512, true>(a, s);
-        case 1024: return mma::launch_mma_m<4, 1024, true>(a, s);
-        case 2048: return mma::launch_mma_m<4, 2048, true>(a, s);
-        case 4096: return mma::launch_mma_m<4, 4096, true>(a, s);
+        case 512: return mma::launch_mma_m<mma::kFmtPackedLdg, 512, true>(a, s);
+        case 1024: return mma::launch_mma_m<mma::kFmtPackedLdg, 1024, true>(a, s);
+        case 2048: return mma::launch_mma_m<mma::kFmtPackedLdg, 2048, true>(a, s);
+        case 4096:
+            if (mma::packed_use_ring(a)) {
+                if (a.M <= 1) return mma::launch_mma<mma::kFmtPackedRing, 4096, 1, true>(a, s);
+                if (a.M <= 2) return mma::launch_mma<mma::kFmtPackedRing, 4096, 2, true>(a, s);
+                return mma::launch_mma<mma::kFmtPackedRing, 4096, 4, true>(a, s);
+            }
+            return mma::launch_mma_m<mma::kFmtPackedLdg, 4096, true>(a, s);
         default: return cudaErrorInvalidValue;
     }
 }

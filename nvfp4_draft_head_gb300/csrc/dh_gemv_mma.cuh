@@ -12,10 +12,13 @@
 // Work split. A tile is 16 head rows x the whole K. One CTA of NW warps owns a
 // tile at a time (tiles blockIdx.x, blockIdx.x + grid, ...); warp w owns the
 // 128-wide k-windows w, w + NW, ... of every tile, so its slice of h stays in
-// registers for the whole kernel (in shared memory at 4 and 8 drafts). Thread (g = lane/4, t = lane%4) loads, for
-// head rows g and g+8 of the tile, the 32 consecutive k of each of its windows
-// starting at 32 t (one 16-byte load per row for NVFP4). Loads of the next
-// P-1 tiles are in flight while a tile is computed. Per-warp partial logits go
+// registers for the whole kernel (in shared memory at 4 and 8 drafts). Thread
+// (g = lane/4, t = lane%4) takes, for head rows g and g+8 of the tile, the 32
+// consecutive k of each of its windows starting at 32 t (16 bytes per row for
+// NVFP4). The packed NVFP4 head at up to four drafts streams through a
+// shared-memory ring of whole tiles that one producer thread fills with 1-D
+// bulk copies, its first tiles before the grid-dependency wait; every other
+// kernel keeps the loads of the next P-1 tiles in flight in registers. Per-warp partial logits go
 // to a ring of RS shared-memory slots guarded by mbarriers; reducer warps sum
 // the NW partials of each (row, draft) in a fixed order (two drafts per
 // float2 read at 16 drafts), keep the best (logit, id or row) key of each, or
@@ -46,6 +49,8 @@
 // activation scale, the reducer's sum by the head's scale.
 #pragma once
 
+#include <atomic>
+
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -58,7 +63,6 @@ namespace mma {
 
 // Registers per thread for tile loads in flight plus the h fragments.
 constexpr int kLoadRegBudget = 64;
-// Compute warps per CTA at most.
 constexpr int kMaxComputeWarps = 20;
 
 constexpr int cmin(int a, int b) { return a < b ? a : b; }
@@ -71,21 +75,37 @@ constexpr int largest_divisor_at_most(int n, int cap) {
 }
 constexpr int cmax(int a, int b) { return a > b ? a : b; }
 
+constexpr int cclamp(int v, int lo, int hi) { return v < lo ? lo : (v > hi ? hi : v); }
 // Tiles per CTA whose dh_idx entries the reducer stages in shared memory
 // (a 64,064-row head on 152 SMs gives 27, a 98,304-row head 41); further
 // tiles read dh_idx from global memory.
 constexpr int kIdCap = 48;
 
+// Kernel variants of the packed NVFP4 head (DH_FMT_NVFP4_PACKED): the
+// shared-memory ring (template format 4) and register loads (format 6); the
+// launcher picks one per call (packed_use_ring).
+constexpr int kFmtPackedRing = 4;
+constexpr int kFmtPackedLdg = 6;
+
 template <int FMT, int K, int MT>
 struct Cfg {
     static constexpr int NWIN = K / 128;                     // 128-wide k-windows per row
-    static constexpr int NW = largest_divisor_at_most(NWIN, kMaxComputeWarps);  // compute warps per CTA
-    static constexpr int WPW = NWIN / NW;                    // windows per warp
-    static constexpr int NT = MT <= 8 ? 1 : 2;               // n8 tiles of drafts
-    static constexpr bool NV = (FMT == 1 || FMT == 4);       // NVFP4 (canonical or packed layout)
-    static constexpr bool PACKED = (FMT == 4);                // tile-major NVFP4 layout
+    static constexpr bool PACKED = (FMT == kFmtPackedRing || FMT == kFmtPackedLdg);  // tile-major NVFP4 layout
+    static constexpr bool NV = (FMT == 1 || PACKED);          // NVFP4 (canonical or packed layout)
     static constexpr bool BLOCKDIAG = (NV && MT == 1);
     static constexpr bool W8A8 = (FMT == 5);                  // FP8 head, FP8 activations
+    // Packed layout, K = 2560, one or two drafts: two CTAs per SM, each of 10
+    // compute warps that own two windows apiece. When one CTA of a launch
+    // retires, a CTA of the next launch takes its place and starts streaming
+    // while the other finishes, and each warp's per-tile hand-off and shuffles
+    // cover two windows. Measured (one draft, 1,000 graph steps): 18.0 -> 17.0
+    // µs top tokens, 19.8 -> 18.4 compute_logits; at 4 drafts and more the
+    // 80-register cap of two CTAs per SM spills.
+    static constexpr bool TWO_CTA = FMT == kFmtPackedRing && MT <= 2 && NWIN == 20;
+    static constexpr int NW = largest_divisor_at_most(NWIN, TWO_CTA ? 10 : kMaxComputeWarps);  // compute warps
+    static constexpr int WPW = NWIN / NW;                    // windows per warp
+    static constexpr int MINB = TWO_CTA ? 2 : 1;             // CTAs per SM the registers must allow
+    static constexpr int NT = MT <= 8 ? 1 : 2;               // n8 tiles of drafts
     static constexpr bool HINT = MT <= 2;                      // suspend-time hint on pipeline waits
     // tiles per CTA at least: 2 for the packed NVFP4 head at K <= 512, whose short
     // tiles leave the step latency-bound (fewer CTAs to hand the argmax over);
@@ -107,36 +127,66 @@ struct Cfg {
     // tiles in flight; spills with three). Packed layout only: the canonical
     // layout's scale ring owns the dynamic shared memory.
     static constexpr bool SMB = PACKED && !BLOCKDIAG && WPW == 1 && (MT == 4 || MT == 8);
-    // tiles of loads in flight in registers: as many as fit, next to the h
-    // fragments (16 registers per window and n8 tile), in the 80 registers that
-    // 21+ warps per SM allow, up to a cap: three with one window per warp and
-    // one n8 tile, two at 16 drafts, one with two windows per warp (K = 4096,
-    // 5120). The packed NVFP4 head (9 registers a tile) measured best with two
-    // at one draft (20.00 -> 19.94 µs top tokens, 22.14 -> 21.76 compute_logits
-    // against three), four at two and eight drafts (21.43 -> 20.99, 22.19 ->
-    // 21.55 against three; four at four drafts was slower) and two at 16
-    // (three spilled: 27.5 -> 33.4). The FP8 heads (16 registers a tile) take
-    // two at every draft count (98,304 rows, one draft: W8A16, where three
-    // spilled, 41.65 -> 40.66 µs top tokens and 44.14 -> 42.64 compute_logits;
-    // W8A8 39.90 -> 39.18 and 42.64 -> 41.76; W8A8 top tokens at four drafts
-    // 40.78 -> 40.98, its compute_logits 44.66 -> 43.95).
+    // Register-load kernels: tiles of loads in flight in registers, as many as
+    // fit next to the h fragments (16 registers per window and n8 tile) in the
+    // 80 registers that 21+ warps per SM allow, up to a cap: three with one n8
+    // tile, two at 16 drafts and for the FP8 heads (98,304 rows, one draft:
+    // W8A16, where three spilled, 41.65 -> 40.66 µs top tokens and 44.14 ->
+    // 42.64 compute_logits; W8A8 39.90 -> 39.18 and 42.64 -> 41.76); the
+    // packed NVFP4 head (9 registers a tile) two at one draft (20.00 -> 19.94
+    // µs against three), four at two and eight drafts (21.43 -> 20.99, 22.19 ->
+    // 21.55; four at four drafts was slower), two at 16 (three spilled).
     static constexpr int PCAP = PACKED ? (MT == 1 ? 2 : (MT == 2 ? 4 : (MT >= 16 ? 2 : 3)))
                                        : ((MT >= 16 || FMT == 2 || FMT == 5) ? 2 : 3);
-    static constexpr int P = SMB ? (MT == 8 ? 4 : 3) : cmax(1, cmin(PCAP, (kLoadRegBudget - WPW * NT * 16) / TILE_REGS));
+    // Packed layout: the head streams through a ring of whole tiles in shared
+    // memory, filled by one producer thread with 1-D bulk copies (the tiles of
+    // this layout are contiguous). Its first RPRE tiles are issued before the
+    // grid-dependency wait, so a launch reads its head while the preceding
+    // kernel in the stream finishes; compute warps then read their windows of
+    // each tile from shared memory, one tile ahead of the math with one window
+    // per warp (P = 2). Issuing more tiles before the wait delays the
+    // preceding launch's hand-off and this launch's first tiles behind the
+    // burst (one draft, one CTA per SM: eight 18.0, four 17.3 µs; two CTAs per
+    // SM: four 17.7, one 17.0).
+    static constexpr bool RING = FMT == kFmtPackedRing;
+    static constexpr int TB = NWIN * WBLK;                    // packed: bytes of one tile
+    static constexpr int RPRE = TWO_CTA ? 1 : 4;
+    static constexpr int P = RING ? ((WPW == 1 && MT <= 8) ? 2 : 1)
+                                  : (SMB ? (MT == 8 ? 4 : 3)
+                                         : cmax(1, cmin(PCAP, (kLoadRegBudget - WPW * NT * 16) / TILE_REGS)));
     // Canonical NVFP4 layout: a loader warp streams each tile's scale bytes
     // into a shared-memory ring with 1-D bulk copies.
     static constexpr bool SCALES = (FMT == 1);
     static constexpr bool LOADER = SCALES;
     // reducer unit: one row and DV drafts (one float2 read per partial at 16 drafts)
     static constexpr int DV = MT >= 16 ? 2 : 1;
+    // One draft: the partial sums are stored row-major ([slot][row][warp]), so
+    // a reducer lane reads its row's partials with 16-byte loads and sums them
+    // as a tree (one draft 21.3 -> 19.7 µs against the warp-major layout with
+    // a sequential sum, where the single reducer warp fell behind).
+    static constexpr bool RED_T = BLOCKDIAG;
     static constexpr int NRW = MT >= 16 ? (16 * MT / DV) / 32 : (MT >= 8 ? 4 : (MT >= 4 ? 2 : 1));  // reducer warps
-    static constexpr int THREADS = (NW + NRW + (LOADER ? 1 : 0)) * 32;  // + reducers (+ loader)
+    static constexpr int THREADS = (NW + NRW + ((LOADER || RING) ? 1 : 0)) * 32;  // + reducers (+ loader / producer)
     static constexpr int SLOT = 16 * SFB;                              // bytes of one ring slot
     static constexpr int SS = 6;
-    // partial-sum slots: eight for the packed one-draft kernels (one draft 19.87 ->
-    // 19.73 µs top tokens, 21.59 -> 21.41 compute_logits against four), else four
-    // while they fit in 40 KB, else two
-    static constexpr int RS = (PACKED && MT == 1) ? 8 : ((4 * NW * 16 * MT * 4 <= 40 * 1024) ? 4 : 2);
+    // partial-sum slots: register-load kernels eight for the packed one-draft
+    // kernel (one draft 19.87 -> 19.73 µs against four), else four while they
+    // fit in 40 KB, else two; the ring kernels as many as their budget holds
+    // (2 to 16), in dynamic shared memory
+    static constexpr int PART_SLOT = NW * 16 * MT * 4;                 // bytes of one partial-sum slot
+    static constexpr int PART_BUDGET = TWO_CTA ? 10 * 1024 : 40 * 1024;
+    static constexpr int RS = RING ? cclamp(PART_BUDGET / PART_SLOT, 2, 16)
+                                   : ((PACKED && MT == 1) ? 8 : ((4 * NW * 16 * MT * 4 <= 40 * 1024) ? 4 : 2));
+    static constexpr int PART_DYN = RING ? RS * PART_SLOT : 0;
+    static constexpr int SMB_BYTES = SMB ? NW * NT * 8 * 32 * 8 : 0;
+    // packed layout: dynamic shared memory of a CTA (one or two per SM) and
+    // the tiles of its ring, as many as fit next to the partials and the h
+    // fragments, 2 to 8
+    static constexpr int RING_BUDGET = TWO_CTA ? 96 * 1024 : 200 * 1024;
+    static constexpr int RT = RING ? cclamp((RING_BUDGET - PART_DYN - SMB_BYTES) / TB, 2, 8) : 0;
+    static constexpr int NSB = RING ? RT : SS;                         // tile / scale ring barriers
+    static constexpr size_t DYN_SMEM = RING ? static_cast<size_t>(RT) * TB + PART_DYN + SMB_BYTES
+                                            : (LOADER ? static_cast<size_t>(SS) * SLOT : static_cast<size_t>(SMB_BYTES));
     static_assert(NWIN % NW == 0, "windows must split evenly over warps");
     static_assert(K % 128 == 0, "K must be a multiple of 128");
 };
@@ -232,19 +282,31 @@ __device__ __forceinline__ uint32_t word_of(const uint4 (&v)[CPR], int i) {
 }
 
 template <int FMT, int K, int MT, bool LOGITS>
-__global__ void __launch_bounds__(Cfg<FMT, K, MT>::THREADS, 1) gemv_mma_kernel(const GemvArgs a) {
+__global__ void __launch_bounds__(Cfg<FMT, K, MT>::THREADS, Cfg<FMT, K, MT>::MINB) gemv_mma_kernel(const GemvArgs a) {
     using C = Cfg<FMT, K, MT>;
     constexpr int NW = C::NW, WPW = C::WPW, NT = C::NT, P = C::P, KW = K / 2, RS = C::RS;
     constexpr int NRED = 16 * MT;  // (row, draft) results of a tile
-    __shared__ __align__(16) float s_part[RS][NW][16][MT];
+    constexpr int RTm = C::RT > 0 ? C::RT : 1;
+    __shared__ __align__(16) float s_part_st[C::RING ? 1 : RS][NW][16][MT];
     __shared__ __align__(8) uint64_t full_p[RS];
     __shared__ __align__(8) uint64_t empty_p[RS];
-    __shared__ __align__(8) uint64_t full_s[C::SS];
-    __shared__ __align__(8) uint64_t empty_s[C::SS];
-    extern __shared__ __align__(16) uint8_t s_scales[];  // [SS][16 rows][K/16] (canonical NVFP4)
+    __shared__ __align__(8) uint64_t full_s[C::NSB];   // tile ring (packed) / scale ring (canonical)
+    __shared__ __align__(8) uint64_t empty_s[C::NSB];
+    // dynamic shared memory: packed layout [RT tiles][RS partial-sum slots][h
+    // fragments]; canonical NVFP4 [SS][16 rows][K/16] scale bytes; otherwise
+    // the h fragments (4 and 8 drafts)
+    extern __shared__ __align__(128) uint8_t s_dyn[];
+    float* const s_part = C::RING ? reinterpret_cast<float*>(s_dyn + static_cast<size_t>(C::RT) * C::TB)
+                                  : &s_part_st[0][0][0][0];
+    // partial sum of (ring slot, compute warp, tile row, draft)
+    auto part = [&](int slot, int w, int row, int m) -> float* {
+        if constexpr (C::RED_T) return s_part + (slot * 16 + row) * NW + w;
+        return s_part + ((slot * NW + w) * 16 + row) * MT + m;
+    };
     __shared__ unsigned long long s_best[NRED];
     __shared__ unsigned long long s_cta[MT];
     __shared__ int s_abort;
+    __shared__ unsigned int s_epoch;  // top-tokens mode: the workspace's epoch (slot bank)
     __shared__ float s_amx[C::W8A8 ? NW : 1][16];  // W8A8: per compute warp and draft, max |h|
     // dh_idx of this CTA's first kIdCap tiles: [i][0..15] the rows' ids, [i][16]
     // the id of the row after the tile (copied when that row exists)
@@ -257,10 +319,23 @@ __global__ void __launch_bounds__(Cfg<FMT, K, MT>::THREADS, 1) gemv_mma_kernel(c
     auto tile_of = [&](int i) { return b0 + i * static_cast<int>(gridDim.x); };
     const uint8_t* q = static_cast<const uint8_t*>(a.q);
     volatile int* abort_flag = &s_abort;
+    // Wait for a pipeline barrier phase. The first test does not block and
+    // does not read the shared abort flag; only a wait that has to block
+    // checks it (a CTA whose waits already ran out stops waiting) and records
+    // a timeout.
+    auto pipe_wait = [&](uint64_t* bar, uint32_t parity) -> bool {
+        if (mbar_test(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (mbar_wait<C::HINT>(bar, parity)) return true;
+        atomicOr(&a.ws->error, kDevErrTimeout);
+        *abort_flag = 1;
+        return false;
+    };
 
-    // Issue the first P tiles' loads before anything else (compute warps).
+    // Issue the first P tiles' loads before anything else (compute warps; the
+    // packed layout's producer issues its ring instead, below).
     TileBuf<FMT, K, MT> buf[P];
-    if (warp < NW) {
+    if (!C::RING && warp < NW) {
 #pragma unroll
         for (int p = 0; p < P; ++p)
             if (p < my_tiles) load_tile<FMT, K, MT>(buf[p], q, tile_of(p), warp, g, t);
@@ -271,7 +346,7 @@ __global__ void __launch_bounds__(Cfg<FMT, K, MT>::THREADS, 1) gemv_mma_kernel(c
             mbar_init(&full_p[r], NW);
             mbar_init(&empty_p[r], C::NRW);
         }
-        for (int r = 0; r < C::SS; ++r) {
+        for (int r = 0; r < C::NSB; ++r) {
             mbar_init(&full_s[r], 1);
             mbar_init(&empty_s[r], NW);
         }
@@ -285,11 +360,23 @@ __global__ void __launch_bounds__(Cfg<FMT, K, MT>::THREADS, 1) gemv_mma_kernel(c
         const int slot = i % C::SS;
         const size_t tile = static_cast<size_t>(tile_of(i));
         mbar_arrive_expect_tx(&full_s[slot], C::SLOT);
-        bulk_g2s(s_scales + slot * C::SLOT, a.sf + tile * C::SLOT, C::SLOT, &full_s[slot], pol);
+        bulk_g2s(s_dyn + slot * C::SLOT, a.sf + tile * C::SLOT, C::SLOT, &full_s[slot], pol);
+    };
+    // The producer's copy of tile i of this CTA into ring slot i % RT.
+    auto issue_tile = [&](int i) {
+        const int slot = i % RTm;
+        mbar_arrive_expect_tx(&full_s[slot], C::TB);
+        bulk_g2s(s_dyn + static_cast<size_t>(slot) * C::TB, q + static_cast<size_t>(tile_of(i)) * C::TB, C::TB,
+                 &full_s[slot], pol);
     };
     int issued = 0;
     if (C::LOADER && warp == NW + C::NRW && lane == 0) {
         for (; issued < C::SS && issued < my_tiles; ++issued) issue(issued);
+    }
+    // The packed layout's producer issues its first tiles now: the head does
+    // not depend on the preceding kernel, so these copies overlap its tail.
+    if (C::RING && warp == NW + C::NRW && lane == 0) {
+        for (; issued < cmin(C::RT, C::RPRE) && issued < my_tiles; ++issued) issue_tile(issued);
     }
     // The reducer warps start copying dh_idx for their tiles now: it belongs to
     // the head, so the copies overlap the preceding kernel's tail instead of
@@ -312,7 +399,25 @@ __global__ void __launch_bounds__(Cfg<FMT, K, MT>::THREADS, 1) gemv_mma_kernel(c
     asm volatile("griddepcontrol.launch_dependents;");
     const uint32_t* h32 = reinterpret_cast<const uint32_t*>(a.h);
 
-    if (warp == NW + C::NRW) {
+    if (C::RING && warp == NW + C::NRW) {
+        // ------------------------------------------------------ producer ----
+        // Refills a ring slot as soon as every compute warp has read it.
+        if constexpr (C::RING) {
+            if (lane == 0) {
+                for (int i = issued; i < my_tiles; ++i) {
+                    const int slot = i % RTm;
+                    if (!pipe_wait(&empty_s[slot], ((i / RTm) - 1) & 1)) break;
+                    issue_tile(i);
+                    issued = i + 1;
+                }
+                if (*abort_flag) {  // let the copies already issued land before the CTA exits
+                    for (int i = issued > RTm ? issued - RTm : 0; i < issued; ++i)
+                        (void)mbar_wait<C::HINT>(&full_s[i % RTm], (i / RTm) & 1);
+                }
+            }
+            __syncwarp();
+        }
+    } else if (warp == NW + C::NRW) {
         // -------------------------------------------------- scale loader ----
         // The 16 x K/16 scale bytes of a tile are contiguous (their per-row
         // 8-byte pieces would otherwise cost one L2 request per row and window).
@@ -341,6 +446,7 @@ __global__ void __launch_bounds__(Cfg<FMT, K, MT>::THREADS, 1) gemv_mma_kernel(c
         // best key per (row, draft), or writes the logits; never blocks the
         // compute warps except when it falls RS tiles behind.
         const int rl = (warp - NW) * 32 + lane;  // this reducer thread's first unit
+        if (!LOGITS && rl == 0) s_epoch = load_epoch(a.ws);  // the slot bank of the argmax hand-off
         cp_async_wait_all();  // this thread's dh_idx copies, then everyone's
         if constexpr (C::NRW > 1) named_bar_sync(1, 32 * C::NRW);
         else __syncwarp();
@@ -353,21 +459,18 @@ __global__ void __launch_bounds__(Cfg<FMT, K, MT>::THREADS, 1) gemv_mma_kernel(c
         for (int i = 0; i < my_tiles; ++i) {
             const int slot = i % RS;
             const int tile = tile_of(i);
-            const int r0 = tile * 16;
             // dh_idx of this tile's rows, fetched before waiting for the partials
             int ids_[SLOTS];
 #pragma unroll
             for (int k = 0; k < SLOTS; ++k) {
                 const int u = rl + k * 32 * C::NRW;
-                const int row = r0 + u / UPR;
+                const int row = tile * 16 + u / UPR;
                 ids_[k] = ((LOGITS || a.idx_ascending) && u < NU && row < a.n_kept)
                               ? (i < n_pre ? s_ids[20 * i + u / UPR] : (a.idx ? __ldg(a.idx + row) : row))
                               : row;
             }
-            if (!*abort_flag && !mbar_wait<C::HINT>(&full_p[slot], (i / RS) & 1)) {
-                atomicOr(&a.ws->error, kDevErrTimeout);
-                *abort_flag = 1;
-            }
+            pipe_wait(&full_p[slot], (i / RS) & 1);
+            const int r0 = tile * 16;
 #pragma unroll
             for (int k = 0; k < SLOTS; ++k) {
                 const int u = rl + k * 32 * C::NRW;
@@ -377,20 +480,34 @@ __global__ void __launch_bounds__(Cfg<FMT, K, MT>::THREADS, 1) gemv_mma_kernel(c
                 float v[DV];
 #pragma unroll
                 for (int d = 0; d < DV; ++d) v[d] = 0.0f;
+                if constexpr (C::RED_T && NW % 4 == 0) {
+                    // the row's NW partials are contiguous: four running sums, then a tree
+                    const float4* pr = reinterpret_cast<const float4*>(part(slot, 0, row_t, 0));
+                    float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+                    for (int w4 = 0; w4 < NW / 4; ++w4) {
+                        const float4 q4 = pr[w4];
+                        acc[0] += q4.x;
+                        acc[1] += q4.y;
+                        acc[2] += q4.z;
+                        acc[3] += q4.w;
+                    }
+                    v[0] = (acc[0] + acc[1]) + (acc[2] + acc[3]);
+                } else
 #pragma unroll 4
                 for (int w = 0; w < NW; ++w) {
                     if constexpr (DV == 4) {
-                        const float4 q4 = *reinterpret_cast<const float4*>(&s_part[slot][w][row_t][m0]);
+                        const float4 q4 = *reinterpret_cast<const float4*>(part(slot, w, row_t, m0));
                         v[0] += q4.x;
                         v[1] += q4.y;
                         v[2] += q4.z;
                         v[3] += q4.w;
                     } else if constexpr (DV == 2) {
-                        const float2 q2 = *reinterpret_cast<const float2*>(&s_part[slot][w][row_t][m0]);
+                        const float2 q2 = *reinterpret_cast<const float2*>(part(slot, w, row_t, m0));
                         v[0] += q2.x;
                         v[1] += q2.y;
                     } else {
-                        v[0] += s_part[slot][w][row_t][m0];
+                        v[0] += *part(slot, w, row_t, m0);
                     }
                 }
                 const int row = r0 + row_t;
@@ -567,7 +684,8 @@ __global__ void __launch_bounds__(Cfg<FMT, K, MT>::THREADS, 1) gemv_mma_kernel(c
                 unscale[nt][1] = __shfl_sync(0xFFFFFFFFu, inv, 4 * (2 * t + 1));
             }
         }
-        uint2* s_hb = reinterpret_cast<uint2*>(s_scales) + (C::SMB ? warp * NT * 8 * 32 : 0);  // [nt][i][lane]
+        uint2* s_hb = reinterpret_cast<uint2*>(s_dyn + (C::RING ? static_cast<size_t>(C::RT) * C::TB + C::PART_DYN : 0)) +
+                      (C::SMB ? warp * NT * 8 * 32 : 0);  // [nt][i][lane]
         if constexpr (C::SMB) {
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt)
@@ -575,21 +693,73 @@ __global__ void __launch_bounds__(Cfg<FMT, K, MT>::THREADS, 1) gemv_mma_kernel(c
                 for (int i = 0; i < 8; ++i) s_hb[(nt * 8 + i) * 32 + lane] = make_uint2(hb[0][nt][2 * i], hb[0][nt][2 * i + 1]);
             __syncwarp();
         }
+        // Tile i's codes and scales into registers: from the ring (packed
+        // layout: wait until the tile has landed, read this warp's windows,
+        // free the slot) or with global loads.
+        auto fetch = [&](TileBuf<FMT, K, MT>& b, int i) {
+            if constexpr (C::RING) {
+                const int rs = i % RTm;
+                pipe_wait(&full_s[rs], (i / RTm) & 1);
+                const uint8_t* tl = s_dyn + static_cast<size_t>(rs) * C::TB;
+#pragma unroll
+                for (int ww = 0; ww < WPW; ++ww) {
+                    const uint8_t* blk = tl + (warp + ww * NW) * C::WBLK;
+                    b.c[ww][0][0] = *reinterpret_cast<const uint4*>(blk + g * 64 + 16 * t);
+                    b.c[ww][1][0] = *reinterpret_cast<const uint4*>(blk + (g + 8) * 64 + 16 * t);
+                    b.sp[ww] = *reinterpret_cast<const uint32_t*>(blk + 16 * 64 + 4 * lane);
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&empty_s[rs]);
+            } else {
+                load_tile<FMT, K, MT>(b, q, tile_of(i), warp, g, t);
+            }
+        };
+        if constexpr (C::RING) {
+#pragma unroll
+            for (int p = 0; p < P; ++p)
+                if (p < my_tiles) fetch(buf[p], p);
+        }
+        // Hand tile ti's partial sums to the reducer (wait for the slot to be
+        // free first).
+        auto handoff = [&](int ti, const float (&out)[NT][4]) {
+            const int slot = ti % RS;
+            if (ti >= RS) pipe_wait(&empty_p[slot], ((ti / RS) - 1) & 1);
+            if constexpr (C::BLOCKDIAG) {
+                if (t == 0) {
+                    *part(slot, warp, g, 0) = out[0][0] * unscale[0][0];
+                    *part(slot, warp, g + 8, 0) = out[0][1] * unscale[0][0];
+                }
+            } else {
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    const int m0 = 8 * nt + 2 * t;
+                    if (m0 < MT) {
+                        *part(slot, warp, g, m0) = out[nt][0] * unscale[nt][0];
+                        *part(slot, warp, g + 8, m0) = out[nt][2] * unscale[nt][0];
+                    }
+                    if (m0 + 1 < MT) {
+                        *part(slot, warp, g, m0 + 1) = out[nt][1] * unscale[nt][1];
+                        *part(slot, warp, g + 8, m0 + 1) = out[nt][3] * unscale[nt][1];
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&full_p[slot]);
+        };
+        // Per tile: math, the loads (ring reads) P tiles ahead, hand-off.
         for (int it = 0; it < my_tiles; it += P) {
 #pragma unroll
             for (int p = 0; p < P; ++p) {
                 const int ti = it + p;
                 if (ti >= my_tiles) break;
                 TileBuf<FMT, K, MT>& b = buf[p];
-                const int slot = ti % RS;
+                float out[NT][4];  // block-diagonal: out[0][0..1] = rows g, g+8
+
 
                 if constexpr (C::SCALES) {
                     const int ss = ti % C::SS;
-                    if (!*abort_flag && !mbar_wait<C::HINT>(&full_s[ss], (ti / C::SS) & 1)) {
-                        atomicOr(&a.ws->error, kDevErrTimeout);
-                        *abort_flag = 1;
-                    }
-                    const uint8_t* st = s_scales + ss * C::SLOT;
+                    pipe_wait(&full_s[ss], (ti / C::SS) & 1);
+                    const uint8_t* st = s_dyn + ss * C::SLOT;
 #pragma unroll
                     for (int ww = 0; ww < WPW; ++ww) {
                         const int w = warp + ww * NW;
@@ -599,12 +769,12 @@ __global__ void __launch_bounds__(Cfg<FMT, K, MT>::THREADS, 1) gemv_mma_kernel(c
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&empty_s[ss]);
                 }
-                float out[NT][4];  // block-diagonal: out[0][0..1] = rows g, g+8
                 if constexpr (C::BLOCKDIAG) {
                     float y0 = 0.0f, y1 = 0.0f;
 #pragma unroll
                     for (int ww = 0; ww < WPW; ++ww) {
-                        float d[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+                        // two accumulators (one per half), summed at the end
+                        float dc[2][4] = {{0.0f, 0.0f, 0.0f, 0.0f}, {0.0f, 0.0f, 0.0f, 0.0f}};
                         // MMA i takes byte i (block 2t) and byte 8+i (block 2t+1) of each
                         // row: words (0, 2) feed i < 4, words (1, 3) feed i >= 4.
 #pragma unroll
@@ -619,9 +789,13 @@ __global__ void __launch_bounds__(Cfg<FMT, K, MT>::THREADS, 1) gemv_mma_kernel(c
 #pragma unroll
                             for (int j = 0; j < 4; ++j) {
                                 const int i = 4 * half + j;
-                                mma_f16(d, fg0[j], fh0[j], fg1[j], fh1[j], hb[ww][0][i], hb[ww][0][8 + i]);
+                                mma_f16(dc[half], fg0[j], fh0[j], fg1[j], fh1[j], hb[ww][0][i],
+                                        hb[ww][0][8 + i]);
                             }
                         }
+                        float d[4];
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) d[c] = dc[0][c] + dc[1][c];
 
                         // scales of blocks 2t, 2t+1 (this thread's D columns) of rows g, g+8
                         uint32_t s01g, s01h;
@@ -744,33 +918,8 @@ __global__ void __launch_bounds__(Cfg<FMT, K, MT>::THREADS, 1) gemv_mma_kernel(c
                 }
                 // loads of the tile P steps ahead go into the buffer just consumed
                 const int tn = ti + P;
-                if (tn < my_tiles) load_tile<FMT, K, MT>(buf[p], q, tile_of(tn), warp, g, t);
-                // hand the partials to the reducer (wait for the slot to be free first)
-                if (ti >= RS && !*abort_flag && !mbar_wait<C::HINT>(&empty_p[slot], ((ti / RS) - 1) & 1)) {
-                    atomicOr(&a.ws->error, kDevErrTimeout);
-                    *abort_flag = 1;
-                }
-                if constexpr (C::BLOCKDIAG) {
-                    if (t == 0) {
-                        s_part[slot][warp][g][0] = out[0][0] * unscale[0][0];
-                        s_part[slot][warp][g + 8][0] = out[0][1] * unscale[0][0];
-                    }
-                } else {
-#pragma unroll
-                    for (int nt = 0; nt < NT; ++nt) {
-                        const int m0 = 8 * nt + 2 * t;
-                        if (m0 < MT) {
-                            s_part[slot][warp][g][m0] = out[nt][0] * unscale[nt][0];
-                            s_part[slot][warp][g + 8][m0] = out[nt][2] * unscale[nt][0];
-                        }
-                        if (m0 + 1 < MT) {
-                            s_part[slot][warp][g][m0 + 1] = out[nt][1] * unscale[nt][1];
-                            s_part[slot][warp][g + 8][m0 + 1] = out[nt][3] * unscale[nt][1];
-                        }
-                    }
-                }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&full_p[slot]);
+                if (tn < my_tiles) fetch(buf[p], tn);
+                handoff(ti, out);
             }
         }
     }
@@ -785,7 +934,7 @@ __global__ void __launch_bounds__(Cfg<FMT, K, MT>::THREADS, 1) gemv_mma_kernel(c
             s_cta[tid] = k;
         }
         __syncthreads();
-        finish_argmax(a, s_cta);
+        finish_argmax(a, s_cta, s_epoch);
     }
 }
 
@@ -795,23 +944,26 @@ inline cudaError_t launch_mma(const GemvArgs& a, cudaStream_t s) {
     auto kern = gemv_mma_kernel<FMT, K, MT, LOGITS>;
     const int sms = sm_count();
     if (sms <= 0) return cudaErrorInvalidDevice;
-    const size_t smem = C::LOADER ? static_cast<size_t>(C::SS) * C::SLOT
-                                  : (C::SMB ? static_cast<size_t>(C::NW) * C::NT * 8 * 32 * sizeof(uint2) : 0);
-    static int occ[64] = {0};
+    const size_t smem = C::DYN_SMEM;
+    // CTAs per SM, looked up once per device (first callers on several host
+    // threads may each look it up; they store the same value)
+    static std::atomic<int> occ[64];
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    if (occ[dev] == 0) {
+    int per_sm = occ[dev].load(std::memory_order_relaxed);
+    if (per_sm == 0) {
         e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
         if (e != cudaSuccess) return e;
         int o = 0;
         e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, kern, C::THREADS, smem);
         if (e != cudaSuccess) return e;
-        occ[dev] = o > 0 ? o : 1;
+        per_sm = o > 0 ? o : 1;
+        occ[dev].store(per_sm, std::memory_order_relaxed);
     }
     const int n_tiles = a.N / 16;
-    int blocks = sms * occ[dev];
+    int blocks = sms * per_sm;
     if (blocks > n_tiles) blocks = n_tiles;
     if (blocks > (n_tiles + C::MIN_TILES - 1) / C::MIN_TILES) blocks = (n_tiles + C::MIN_TILES - 1) / C::MIN_TILES;
     if (blocks > kMaxGrid) blocks = kMaxGrid;  // one argmax slot per CTA
@@ -842,6 +994,28 @@ inline cudaError_t launch_mma_m(const GemvArgs& a, cudaStream_t s) {
 template <int FMT, int K>
 inline cudaError_t launch_mma_k(const GemvArgs& a, cudaStream_t s) {
     return a.out ? launch_mma_m<FMT, K, true>(a, s) : launch_mma_m<FMT, K, false>(a, s);
+}
+
+// The ring kernels of the packed head, up to four drafts.
+template <int K>
+inline cudaError_t launch_ring_k(const GemvArgs& a, cudaStream_t s) {
+    if (a.out) {
+        if (a.M <= 1) return launch_mma<kFmtPackedRing, K, 1, true>(a, s);
+        if (a.M <= 2) return launch_mma<kFmtPackedRing, K, 2, true>(a, s);
+        return launch_mma<kFmtPackedRing, K, 4, true>(a, s);
+    }
+    if (a.M <= 1) return launch_mma<kFmtPackedRing, K, 1, false>(a, s);
+    if (a.M <= 2) return launch_mma<kFmtPackedRing, K, 2, false>(a, s);
+    return launch_mma<kFmtPackedRing, K, 4, false>(a, s);
+}
+
+// Packed head: the ring kernel for up to four drafts, K >= 2560, on heads of at
+// least eight tiles per SM or K >= 4096 (one draft, 64,064 x 2560: 19.8 ->
+// 16.9 µs; 4 drafts 21.4 -> 20.4); register loads otherwise (8 and 16 drafts,
+// where the ring measured 0.8 and 2.5 µs slower; the 4,032 x 256 head; the
+// 1,024 - 4,608-row linears at K <= 2560).
+inline bool packed_use_ring(const GemvArgs& a) {
+    return a.M <= 4 && a.K >= 2560 && (a.N / 16 >= 8 * sm_count() || a.K >= 4096);
 }
 
 }  // namespace mma

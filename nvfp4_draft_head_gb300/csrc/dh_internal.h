@@ -24,6 +24,7 @@ struct GemvArgs {
     int M;
     int32_t* ids;        // top-tokens mode
     float* top;          // optional
+    unsigned long long* keys;  // shard-keys mode (instead of ids / top): int64 keys [M]
     float* out;          // logits mode: fp32 [M][V]
     Workspace* ws;
 };
