@@ -38,6 +38,15 @@
  *   - Ids are int32 (V < 2^31); the pages' int64 ids have the same values.
  *   - One call at a time per workspace: two calls in flight on the GPU that
  *     share a workspace race on its argmax slots.
+ *   - Draft steps are launched with programmatic stream serialisation: their
+ *     kernels start reading the head (q, sf, scale, idx) while the kernel
+ *     launched just before them on the same stream may still be running, and
+ *     touch h, the workspace and the outputs only after it has completed. So
+ *     the kernel immediately preceding a draft step on its stream must not
+ *     write that head: after quantising or packing a head on a stream, put any
+ *     other operation (an event record, a copy, a memset such as
+ *     draft_head_workspace_init, another kernel) between it and the first
+ *     draft step, or build the head on another stream and synchronise.
  */
 #ifndef DRAFTHEAD_H
 #define DRAFTHEAD_H
@@ -190,9 +199,13 @@ int nvfp4_pack_head(const uint8_t *q, const uint8_t *sf, int N, int K, uint8_t *
  * part alone. */
 size_t draft_head_workspace_bytes(const dh_head_t *hd, int M_max);
 
-/* Zero a draft-step workspace (error word, per-CTA argmax slots). Call once
- * after allocating it; every later call leaves the slots zeroed again. After
- * a DH_DEVERR_TIMEOUT, call it again before the next draft step. */
+/* Zero a draft-step workspace (error word, epoch, argmax slots). Call once
+ * after allocating it. Draft steps keep it consistent from then on, also
+ * after a DH_DEVERR_TIMEOUT: the per-CTA argmax slots alternate between two
+ * banks from step to step, the collecting CTA zeroes every slot it read, and
+ * a key stored after its collector gave up waiting for it lands in a bank the
+ * next step does not read; that step zeroes it before the bank comes round
+ * again. */
 int draft_head_workspace_init(void *ws, size_t ws_bytes, void *stream);
 
 /* get_top_tokens ("q38_draft.py"): for each draft m < M,
@@ -230,6 +243,35 @@ int draft_head_top_tokens_host(const dh_head_t *hd, const void *h_host, int M, i
 int draft_head_compute_logits(const dh_head_t *hd, const void *h, int M, float *out,
                               void *ws, size_t ws_bytes, void *stream);
 
+/* One shard of a vocabulary-sharded draft head ("q38_draft.py", install:
+ * speculative_config.use_local_argmax_reduction; "FP8 MTP draft stack ...",
+ * ParallelLMHead, which splits the head's rows over ranks). A shard is an
+ * ordinary head whose dh_idx holds the global target ids of its rows, in
+ * strictly ascending order (DH_HEAD_IDX_ASCENDING is required; a BF16 head
+ * without idx counts as ascending). Instead of ids, the draft step writes for
+ * each draft m < M one int64 key
+ *     key[m] = (int64)(((uint64)ord(y*) << 32 | (0xFFFFFFFF - id*)) ^ 2^63)
+ * where (y*, id*) is the shard's best (logit, target id): the largest logit,
+ * among equal logits the lowest id. ord() maps an fp32 value to uint32
+ * preserving order (-0 as +0; every NaN above +inf, as torch.argmax lets NaN
+ * win): u | 2^31 for a non-negative value with bits u, ~u for a negative one.
+ * The signed maximum of the shards' keys is then the key of the whole head's
+ * argmax, so one all-reduce(MAX) of M int64 per step completes the step
+ * (draft_head_keys_to_ids decodes it). keys: device int64 [M], 8-byte aligned.
+ * Other arguments, workspace and errors as draft_head_top_tokens;
+ * DH_ERR_ARG if dh_idx is not flagged ascending. One kernel launch. */
+int draft_head_top_keys(const dh_head_t *hd, const void *h, int M, int64_t *keys, void *ws,
+                        size_t ws_bytes, void *stream);
+
+/* Decode argmax keys (draft_head_top_keys, combined over shards by a MAX
+ * all-reduce) into target ids and, when top_logit is not NULL, the winning
+ * logits: id = 0xFFFFFFFF - (key & 0xFFFFFFFF) after undoing the sign flip,
+ * logit = the fp32 value whose ord() is the key's high word (NaN for the NaN
+ * key). A key of INT64_MIN (no row anywhere) gives id -1. keys: device int64
+ * [M]; ids: device int32 [M]; top_logit: device fp32 [M] or NULL; 1 <= M <= 16.
+ * One kernel launch on `stream`. */
+int draft_head_keys_to_ids(const int64_t *keys, int M, int32_t *ids, float *top_logit, void *stream);
+
 /* NVFP4 W4A16 linear layer of the MTP block ("q38_draft.py", MTP_QUANT_KEYS:
  * fc_embedding, fc_hidden, qkv_proj, o_proj, shared_expert are quantised with
  * the same NVFP4 recipe as the head): for m < M and n < N,
@@ -252,30 +294,42 @@ int nvfp4_linear(const dh_head_t *w, const void *x, int M, float *y, void *ws, s
  * synchronise the device. The paper has no counterpart of this entry point.
  * Same arguments and results as draft_head_top_tokens, minus the workspace.
  * Its scratch is one fixed array inside the library, laid out as a
- * draft-step workspace (argmax slots for at most DH_MAX_M = 16 drafts, an
- * error word; draft_head_workspace_bytes(NULL, 16) bytes); every GPU that loads the
- * library holds it until the process exits. M > 16 returns DH_ERR_SHAPE.
- * The first call on a device looks up the array's device address
- * (cudaGetSymbolAddress) with that device current; make that first call
- * before any stream capture. Each call launches the kernel alone (the slots
- * are zero at load and each launch zeroes them again); nothing is allocated.
- * All calls share the one array, so calls that overlap on the GPU (other
- * streams, other threads) race and give wrong ids: serialise them. An id of
- * -1 marks a winning row whose dh_idx entry was outside [0, V). */
+ * draft-step workspace (two banks of argmax slots for at most DH_MAX_M = 16
+ * drafts, an epoch, an error word; draft_head_workspace_bytes(NULL, 16)
+ * bytes); every GPU that loads the library holds it until the process exits.
+ * M > 16 returns DH_ERR_SHAPE. The first call on a device looks up the
+ * array's device address (cudaGetSymbolAddress) with that device current;
+ * make that first call before any stream capture. Each call launches the
+ * kernel alone; nothing is allocated. The array is zero at load and stays
+ * consistent from step to step, also after a step whose bounded wait ran out
+ * (see draft_head_workspace_init). All calls share the one array, so calls
+ * that overlap on the GPU (other streams, other threads) race and give wrong
+ * ids: serialise them. Device-side faults (a dh_idx entry outside [0, V),
+ * which also gives the id -1; a wait that ran out) set bits in the array's
+ * error word: read and clear it with draft_head_static_read_device_error. */
 int draft_head_top_tokens_static(const dh_head_t *hd, const void *h, int M, int32_t *ids,
                                  float *top_logit, void *stream);
+
+/* Synchronise `stream`, then read and clear the device error word of the
+ * static scratch of draft_head_top_tokens_static on the current device
+ * (DH_DEVERR_* bits; *err = 0 when nothing was recorded). As the first call
+ * on a device, it looks up the array's address like that entry point. */
+int draft_head_static_read_device_error(int *err, void *stream);
 
 /* Self-test of the failure handling of the draft-step kernels (the pages have
  * no counterpart): a one-thread kernel waits for an event that nothing
  * produces and gives up after `rounds` tries, recording DH_DEVERR_TIMEOUT in
  * the error word of `ws` exactly as a draft step whose wait ran out does; the
  * context stays usable. kind 0: polls a word of the workspace header that
- * nothing writes (the argmax hand-off's wait); kind 1: waits on a shared-memory
- * mbarrier that nothing arrives on (the load pipeline's wait).
- * ws: a workspace of at least draft_head_quantize_workspace_bytes() bytes;
- * 1 <= rounds <= 2^22 (a draft step's own limit). Read the result with
- * draft_head_read_device_error. Errors: DH_ERR_ARG (kind, rounds),
- * DH_ERR_WORKSPACE. */
+ * nothing writes (a bounded poll of global memory, the argmax hand-off's
+ * wait); kind 1: waits on a shared-memory mbarrier that nothing arrives on
+ * (the load pipeline's wait).
+ * ws: a workspace of at least draft_head_quantize_workspace_bytes() bytes
+ * (ws_bytes), or NULL for the static scratch of draft_head_top_tokens_static
+ * on the current device (ws_bytes ignored); 1 <= rounds <= 2^22 (a draft
+ * step's own limit). Read the result with draft_head_read_device_error
+ * (draft_head_static_read_device_error for NULL). Errors: DH_ERR_ARG (kind,
+ * rounds), DH_ERR_WORKSPACE. */
 int draft_head_wait_probe(void *ws, size_t ws_bytes, int kind, unsigned int rounds, void *stream);
 
 /* Synchronise `stream`, then read and clear the device error word of `ws`

@@ -12,6 +12,9 @@ Names follow the C ABI in include/drafthead.h:
   DraftHead.top_tokens     get_top_tokens: dh_idx[argmax_n (W_q h)]
   DraftHead.compute_logits compute_logits: -inf row + logits at dh_idx
   NVFP4Linear              nvfp4_linear: an MTP-block linear, y = x W'^T
+  DraftHead.top_keys       draft_head_top_keys: a vocabulary shard's argmax keys
+  keys_to_ids              draft_head_keys_to_ids: combined keys -> target ids
+The vocabulary-sharded head (the local-argmax exchange) is in .sharded.
 """
 from __future__ import annotations
 
@@ -37,7 +40,8 @@ EXPORTS = (
     "draft_head_top_tokens", "draft_head_compute_logits", "draft_head_read_device_error",
     "draft_head_status_string", "draft_head_abi_version", "draft_head_top_tokens_static",
     "nvfp4_pack_head", "fp8_quantize_activations", "draft_head_last_cuda_error", "nvfp4_linear",
-    "draft_head_wait_probe", "draft_head_top_tokens_host",
+    "draft_head_wait_probe", "draft_head_top_tokens_host", "draft_head_top_keys", "draft_head_keys_to_ids",
+    "draft_head_static_read_device_error",
 )
 
 _lib = None
@@ -96,6 +100,9 @@ def lib():
         L.draft_head_last_cuda_error.argtypes = [C.POINTER(C.c_char_p)]
         L.nvfp4_linear.argtypes = [C.POINTER(dh_head_t), P, I, P, P, S, P]
         L.draft_head_wait_probe.argtypes = [P, S, I, C.c_uint, P]
+        L.draft_head_top_keys.argtypes = [C.POINTER(dh_head_t), P, I, P, P, S, P]
+        L.draft_head_keys_to_ids.argtypes = [P, I, P, P, P]
+        L.draft_head_static_read_device_error.argtypes = [P, P]
         _lib = L
     return _lib
 
@@ -204,11 +211,21 @@ def draft_head_read_device_error(ws: torch.Tensor, stream=None) -> int:
     return err.value
 
 
-def draft_head_wait_probe(ws: torch.Tensor, kind: int, rounds: int, stream=None) -> None:
-    """Enqueue the bounded-wait self-test on workspace ws (kind 0: a global
+def draft_head_static_read_device_error(stream=None) -> int:
+    """Read and clear the static scratch's device error word (synchronises)."""
+    err = C.c_int(0)
+    _check("draft_head_static_read_device_error",
+           lib().draft_head_static_read_device_error(C.byref(err), _stream(stream)))
+    return err.value
+
+
+def draft_head_wait_probe(ws: torch.Tensor | None, kind: int, rounds: int, stream=None) -> None:
+    """Enqueue the bounded-wait self-test on workspace ws, or on the static
+    scratch of draft_head_top_tokens_static when ws is None (kind 0: a global
     word nothing writes, 1: an mbarrier nothing arrives on)."""
     _check("draft_head_wait_probe",
-           lib().draft_head_wait_probe(ws.data_ptr(), ws.numel(), kind, rounds, _stream(stream)))
+           lib().draft_head_wait_probe(_ptr(ws), 0 if ws is None else ws.numel(), kind, rounds,
+                                       _stream(stream)))
 
 
 def _raise_device_error(ws, stream, fn):
@@ -271,6 +288,18 @@ class DraftHead:
                                            _stream(stream)))
         return ids
 
+    def top_keys(self, h: torch.Tensor, keys: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+        """This head as one vocabulary shard: int64[M] argmax keys (largest
+        logit, then lowest target id) whose maximum over shards is the whole
+        head's; needs an ascending dh_idx."""
+        M = self._check_h(h)
+        if keys is None:
+            keys = torch.empty(M, dtype=torch.int64, device=h.device)
+        _check("draft_head_top_keys",
+               lib().draft_head_top_keys(C.byref(self.desc), h.data_ptr(), M, keys.data_ptr(),
+                                         self.ws.data_ptr(), self.ws_bytes, _stream(stream)))
+        return keys
+
     def top_tokens_host(self, h: torch.Tensor, ids: torch.Tensor | None = None,
                         top: torch.Tensor | None = None, stream=None) -> torch.Tensor:
         """get_top_tokens on host tensors: h a CPU bfloat16 [M, K] tensor; ids
@@ -311,6 +340,19 @@ class DraftHead:
         if h.dtype != torch.bfloat16 or h.dim() != 2 or h.shape[1] != self.K or not h.is_contiguous():
             raise ValueError(f"h must be a contiguous [M, {self.K}] bfloat16 tensor")
         return h.shape[0]
+
+
+def keys_to_ids(keys: torch.Tensor, ids: torch.Tensor | None = None, top: torch.Tensor | None = None,
+                stream=None) -> torch.Tensor:
+    """Target ids (and, into `top`, the winning logits) of argmax keys."""
+    M = keys.numel()
+    if keys.dtype != torch.int64 or not keys.is_contiguous():
+        raise ValueError("keys must be a contiguous int64 tensor")
+    if ids is None:
+        ids = torch.empty(M, dtype=torch.int32, device=keys.device)
+    _check("draft_head_keys_to_ids",
+           lib().draft_head_keys_to_ids(keys.data_ptr(), M, ids.data_ptr(), _ptr(top), _stream(stream)))
+    return ids
 
 
 def nvfp4_head(W: torch.Tensor, keep, packed: bool = True, stream=None) -> DraftHead:

@@ -212,6 +212,27 @@ int draft_head_top_tokens(const dh_head_t* hd, const void* h, int M, int32_t* id
     return cuda_status(dh::launch_gemv(a, static_cast<cudaStream_t>(stream)));
 }
 
+int draft_head_top_keys(const dh_head_t* hd, const void* h, int M, int64_t* keys, void* ws, size_t ws_bytes,
+                        void* stream) {
+    int st = dh::check_step_args(hd, h, M);
+    if (st != DH_OK) return st;
+    if (keys == nullptr) return DH_ERR_ARG;
+    if (hd->idx != nullptr && !(hd->flags & DH_HEAD_IDX_ASCENDING)) return DH_ERR_ARG;  // keys carry ids
+    if (!aligned(keys, 8)) return DH_ERR_ALIGN;
+    if ((st = check_ws(ws, ws_bytes, sizeof(dh::Workspace))) != DH_OK) return st;
+    dh::GemvArgs a = dh::step_args(hd, h, M, ws);
+    a.keys = reinterpret_cast<unsigned long long*>(keys);
+    return cuda_status(dh::launch_gemv(a, static_cast<cudaStream_t>(stream)));
+}
+
+int draft_head_keys_to_ids(const int64_t* keys, int M, int32_t* ids, float* top_logit, void* stream) {
+    if (keys == nullptr || ids == nullptr) return DH_ERR_ARG;
+    if (M < 1 || M > DH_MAX_M) return DH_ERR_SHAPE;
+    if (!aligned(keys, 8) || !aligned(ids, 4) || (top_logit && !aligned(top_logit, 4))) return DH_ERR_ALIGN;
+    return cuda_status(dh::launch_keys_to_ids(reinterpret_cast<const unsigned long long*>(keys), M, ids, top_logit,
+                                              static_cast<cudaStream_t>(stream)));
+}
+
 int draft_head_top_tokens_host(const dh_head_t* hd, const void* h_host, int M, int32_t* ids_host, float* top_host,
                                void* ws, size_t ws_bytes, void* stream) {
     int st = check_head(hd);
@@ -277,10 +298,14 @@ int nvfp4_linear(const dh_head_t* w, const void* x, int M, float* y, void* ws, s
 }
 
 int draft_head_wait_probe(void* ws, size_t ws_bytes, int kind, unsigned int rounds, void* stream) {
-    int st = check_ws(ws, ws_bytes, dh::kWorkspaceHeader);
-    if (st != DH_OK) return st;
     if (kind != 0 && kind != 1) return DH_ERR_ARG;
     if (rounds < 1 || rounds > (1u << 22)) return DH_ERR_ARG;
+    int st;
+    if (ws == nullptr) {  // the static scratch of draft_head_top_tokens_static
+        if ((st = dh::static_scratch_address(&ws)) != DH_OK) return st;
+    } else if ((st = check_ws(ws, ws_bytes, dh::kWorkspaceHeader)) != DH_OK) {
+        return st;
+    }
     return cuda_status(dh::launch_wait_probe(static_cast<dh::Workspace*>(ws), kind, rounds,
                                              static_cast<cudaStream_t>(stream)));
 }

@@ -28,6 +28,22 @@ __global__ void fill_neg_inf_kernel(float4* out4, size_t n4, float* tail, int nt
 }
 
 
+// Shard keys -> ids ("q38_draft.py", install: the local-argmax reduction ends
+// with the winning id). The key's sign bit was flipped so that signed order
+// equals the unsigned order of (ordered logit << 32 | ~id).
+__global__ void keys_to_ids_kernel(const unsigned long long* keys, int M, int32_t* ids, float* top) {
+    const int m = threadIdx.x;
+    if (m >= M) return;
+    const unsigned long long k = keys[m] ^ 0x8000000000000000ull;
+    ids[m] = k == 0ull ? -1 : static_cast<int32_t>(0xFFFFFFFFu - static_cast<uint32_t>(k & 0xFFFFFFFFull));
+    if (top) top[m] = k == 0ull ? __uint_as_float(0x7FC00000u) : ordered_value(static_cast<uint32_t>(k >> 32));
+}
+
+cudaError_t launch_keys_to_ids(const unsigned long long* keys, int M, int32_t* ids, float* top, cudaStream_t s) {
+    keys_to_ids_kernel<<<1, 32, 0, s>>>(keys, M, ids, top);
+    return cudaGetLastError();
+}
+
 // Self-test of the bounded waits: wait for an event that never happens (kind
 // 0: a workspace word nothing writes, polled like the argmax hand-off's slots;
 // kind 1: an mbarrier nothing arrives on, waited on like the pipeline's), give

@@ -106,7 +106,10 @@ struct Cfg {
     static constexpr int WPW = NWIN / NW;                    // windows per warp
     static constexpr int MINB = TWO_CTA ? 2 : 1;             // CTAs per SM the registers must allow
     static constexpr int NT = MT <= 8 ? 1 : 2;               // n8 tiles of drafts
-    static constexpr bool HINT = MT <= 2;                      // suspend-time hint on pipeline waits
+    // suspend-time hint on pipeline waits: register-load kernels at one and
+    // two drafts (measured faster there); the ring kernels wait without it
+    // (one draft 16.98 -> 16.90 µs)
+    static constexpr bool HINT = MT <= 2 && FMT != kFmtPackedRing;
     // tiles per CTA at least: 2 for the packed NVFP4 head at K <= 512, whose short
     // tiles leave the step latency-bound (fewer CTAs to hand the argmax over);
     // measured slower for K >= 2560 linears and no better for the FP8 head

@@ -44,6 +44,10 @@ cudaError_t launch_gemv(const GemvArgs& a, cudaStream_t s);
 // tile-major layout of DH_FMT_NVFP4_PACKED (N % 16 == 0, K % 128 == 0).
 cudaError_t launch_nvfp4_pack(const uint8_t* q, const uint8_t* sf, int N, int K, uint8_t* out, cudaStream_t s);
 
+// Decode M shard keys (signed-order int64, see draft_head_top_keys) into ids
+// and optional top logits. One single-warp kernel.
+cudaError_t launch_keys_to_ids(const unsigned long long* keys, int M, int32_t* ids, float* top, cudaStream_t s);
+
 // Fill out[0..count) with -inf.
 cudaError_t launch_fill_neg_inf(float* out, size_t count, cudaStream_t s);
 
@@ -66,6 +70,10 @@ cudaError_t launch_wait_probe(Workspace* ws, int kind, uint32_t rounds, cudaStre
 // (ids, top and out left empty).
 int check_step_args(const struct dh_head* hd, const void* h, int M);
 GemvArgs step_args(const struct dh_head* hd, const void* h, int M, void* ws);
+
+// Device address of the static scratch of draft_head_top_tokens_static on the
+// current device (looked up on first use): DH_OK or a dh_status.
+int static_scratch_address(void** out);
 
 // Remember e as the calling thread's last CUDA error (draft_head_last_cuda_error)
 // and return DH_ERR_CUDA.

@@ -4,6 +4,7 @@
 // synchronise the device). Its scratch (the per-draft, per-CTA argmax slots
 // and the device error word) lives in a fixed array of this library instead
 // of a caller-provided workspace.
+#include <atomic>
 #include <cstddef>
 #include <cstdint>
 #include <cuda_runtime.h>
@@ -14,15 +15,18 @@
 
 namespace {
 
-// Scratch laid out as a draft-step workspace: the error word and argmax slots
-// for up to DH_MAX_M drafts (zero at load; each launch zeroes the slots it
-// used again). Every GPU that loads the library holds it until the process
-// exits. In host code this name is only a host-side stand-in for the array:
-// the device address comes from cudaGetSymbolAddress.
+// Scratch laid out as a draft-step workspace: the error word, the epoch and
+// the two banks of argmax slots for up to DH_MAX_M drafts (zero at load; each
+// step zeroes the slots it read, and a step whose wait ran out leaves its bank
+// to the next step to zero). Every GPU that loads the library holds it until
+// the process exits. In host code this name is only a host-side stand-in for
+// the array: the device address comes from cudaGetSymbolAddress.
 static __device__ __align__(256) unsigned char g_static_scratch[sizeof(dh::Workspace)];
 
 constexpr int kMaxDevices = 64;
-void* g_scratch_addr[kMaxDevices] = {nullptr};
+// the array's device address per device; first callers on several host
+// threads may each look it up and store the same value
+std::atomic<void*> g_scratch_addr[kMaxDevices];
 
 // Device address of the scratch array on the current device, looked up once
 // per device (with that device current).
@@ -31,18 +35,28 @@ int static_scratch(void** out) {
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return dh::record_cuda_error(e);
     if (dev < 0 || dev >= kMaxDevices) return dh::record_cuda_error(cudaErrorInvalidDevice);
-    if (g_scratch_addr[dev] == nullptr) {
-        void* p = nullptr;
+    void* p = g_scratch_addr[dev].load(std::memory_order_acquire);
+    if (p == nullptr) {
         e = cudaGetSymbolAddress(&p, g_static_scratch);
         if (e != cudaSuccess) return dh::record_cuda_error(e);
         if (p == nullptr) return dh::record_cuda_error(cudaErrorInvalidSymbol);
-        g_scratch_addr[dev] = p;
+        g_scratch_addr[dev].store(p, std::memory_order_release);
     }
-    *out = g_scratch_addr[dev];
+    *out = p;
     return DH_OK;
 }
 
 }  // namespace
+
+int dh::static_scratch_address(void** out) { return static_scratch(out); }
+
+extern "C" int draft_head_static_read_device_error(int* err, void* stream) {
+    if (err == nullptr) return DH_ERR_ARG;
+    void* scratch = nullptr;
+    int st = static_scratch(&scratch);
+    if (st != DH_OK) return st;
+    return draft_head_read_device_error(scratch, err, stream);
+}
 
 extern "C" int draft_head_top_tokens_static(const dh_head_t* hd, const void* h, int M, int32_t* ids,
                                             float* top_logit, void* stream) {

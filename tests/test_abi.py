@@ -226,7 +226,9 @@ def test_linear_rejects_bad_arguments(L, kw, M, status):
 
 
 def test_wait_probe_rejects_bad_arguments(L):
-    assert L.draft_head_wait_probe(None, 256, 0, 16, None) == dh.DH_ERR_ARG
+    # NULL selects the static scratch; kind and rounds are checked first
+    assert L.draft_head_wait_probe(None, 0, 2, 16, None) == dh.DH_ERR_ARG
+    assert L.draft_head_wait_probe(None, 0, 0, 0, None) == dh.DH_ERR_ARG
     assert L.draft_head_wait_probe(WS + 16, 256, 0, 16, None) == dh.DH_ERR_WORKSPACE
     assert L.draft_head_wait_probe(WS, 128, 0, 16, None) == dh.DH_ERR_WORKSPACE
     assert L.draft_head_wait_probe(WS, 256, 2, 16, None) == dh.DH_ERR_ARG

@@ -566,3 +566,34 @@ def test_out_of_range_idx_sets_the_error_word(tiny):
     assert head_bad_asc.device_error() == dh.DH_DEVERR_IDX
     with pytest.raises(RuntimeError, match="device error"):
         dh.nvfp4_quantize_rows(dev_bf16(tiny.W), idx_bad)
+
+
+def test_late_argmax_key_never_reaches_a_later_step(tiny):
+    """A key stored after its step's collector gave up waiting lands in that
+    step's slot bank, and the step marks the bank dirty. Simulated here by
+    writing huge keys over the whole previous bank and the dirty word: the next
+    steps (which alternate banks) return the oracle's ids, the next one zeroes
+    the dirty bank and clears the mark, and the epoch advances once per step."""
+    head, _ = gpu_nvfp4(tiny, packed=True)
+    q_o, sf_o, g_o = tiny.nvfp4()
+    M = 3
+    h0 = syn.hidden_bf16(syn.hidden_seed(0, 8100), M, tiny.K)
+    head.top_tokens(dev_bf16(h0))
+    torch.cuda.synchronize()
+    hdr = head.ws[:256].view(torch.int32)
+    slots = head.ws[256:256 + 2 * 16 * 1024 * 8].view(torch.int64).view(2, 16, 1024)
+    epoch = int(hdr[2].item())
+    prev = (epoch - 1) & 1
+    slots[prev].fill_(0x7FFFFFFFFFFFFFFF)
+    hdr[3] = 1 | (prev << 1) | (16 << 2) | (1024 << 8)
+    torch.cuda.synchronize()
+    for step in range(4):
+        hb = syn.hidden_bf16(syn.hidden_seed(0, 8101 + step), M, tiny.K)
+        ids = head.top_tokens(dev_bf16(hb)).cpu().numpy()
+        y, A = oracle.gemv(oracle.FMT_NVFP4, q_o, sf_o, g_o, hb)
+        check_argmax_rows(ids_to_rows(ids, tiny.idx, tiny.n_kept), y, A, tiny.n_kept, f"late key, step {step}")
+        if step == 0:
+            assert int(hdr[3].item()) == 0
+            assert int(slots[prev].abs().sum().item()) == 0
+    assert int(hdr[2].item()) == epoch + 4
+    assert head.device_error() == 0

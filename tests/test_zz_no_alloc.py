@@ -79,3 +79,32 @@ def test_static_scratch_entry_point_runs_the_w8a8_head():
                                               None, stream) == dh.DH_OK
         torch.cuda.synchronize()
         assert np.array_equal(ids_ws.cpu().numpy(), ids_st.cpu().numpy()), call
+
+
+def test_static_scratch_reports_a_timed_out_wait_and_runs_on():
+    """A bounded wait that runs out on the static scratch (the self-test probe,
+    as a draft step whose wait ran out) sets its error word, which
+    draft_head_static_read_device_error reads and clears; the next static
+    draft step still matches the workspace entry point."""
+    from nvfp4_draft_head_gb300 import build
+    build.build()
+    L = dh.lib()
+    c = syn.TINY
+    W = syn.head_bf16(syn.SEED_HEAD_TINY, c["V"], c["K"])
+    keep = syn.keep_mask(syn.SEED_KEEP_TINY, c["V"], c["n_kept"], c["forced"])
+    Wd = torch.from_numpy(W.view(np.int16)).cuda().view(torch.bfloat16)
+    head = dh.nvfp4_head(Wd, keep)
+    stream = torch.cuda.current_stream().cuda_stream
+    assert dh.draft_head_static_read_device_error() == 0
+    for kind, rounds in ((0, 1 << 14), (1, 1 << 11)):
+        dh.draft_head_wait_probe(None, kind, rounds)
+        assert dh.draft_head_static_read_device_error() == dh.DH_DEVERR_TIMEOUT, kind
+        assert dh.draft_head_static_read_device_error() == 0
+        M = 4
+        hb = syn.hidden_bf16(syn.hidden_seed(0, 7200 + kind), M, c["K"])
+        h = torch.from_numpy(hb.view(np.int16)).cuda().view(torch.bfloat16)
+        ids_st = torch.full((M,), -7, dtype=torch.int32, device="cuda")
+        assert L.draft_head_top_tokens_static(C.byref(head.desc), h.data_ptr(), M, ids_st.data_ptr(),
+                                              None, stream) == dh.DH_OK
+        assert np.array_equal(head.top_tokens(h).cpu().numpy(), ids_st.cpu().numpy()), kind
+        assert dh.draft_head_static_read_device_error() == 0
