@@ -31,6 +31,8 @@ struct Workspace {
 };
 constexpr size_t kWorkspaceHeader = 256;
 static_assert(offsetof(Workspace, slots) == kWorkspaceHeader, "workspace header is 256 bytes");
+static_assert(offsetof(Workspace, epoch) % 8 == 0 && offsetof(Workspace, dirty) == offsetof(Workspace, epoch) + 4,
+              "epoch and dirty are read together");
 
 constexpr unsigned int kDevErrIdx = 1u;
 

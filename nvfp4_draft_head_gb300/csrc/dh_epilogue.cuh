@@ -9,12 +9,13 @@
 
 namespace dh {
 
-// Epoch of the workspace, read by every CTA after the grid-dependency wait
-// (the preceding step has completed, so its epoch advance is visible).
-__device__ __forceinline__ unsigned int load_epoch(const Workspace* ws) {
-    unsigned int e;
-    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(e) : "l"(&ws->epoch) : "memory");
-    return e;
+// Epoch and dirty word of the workspace (adjacent), read by every CTA after
+// the grid-dependency wait (the preceding step has completed, so its updates
+// are visible), early, so that the hand-off at the end does not wait for them.
+__device__ __forceinline__ uint2 load_epoch_dirty(const Workspace* ws) {
+    uint2 v;
+    asm volatile("ld.relaxed.gpu.global.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(&ws->epoch) : "memory");
+    return v;
 }
 
 // Grid-wide argmax hand-off. Every CTA stores its best key per draft in its
@@ -27,8 +28,9 @@ __device__ __forceinline__ unsigned int load_epoch(const Workspace* ws) {
 // late CTA's store still lands there, before this launch completes. The next
 // step collects from the other bank and zeroes the dirty one, so a late key
 // never reaches a later step.
+// The workspace's epoch and dirty word were read at the kernel's start.
 __device__ __forceinline__ void finish_argmax(const GemvArgs& a, const unsigned long long* cta_key,
-                                              unsigned int epoch) {
+                                              unsigned int epoch, unsigned int dirty) {
     const unsigned int bank = epoch & 1u;
     if (threadIdx.x < a.M) {
         const unsigned long long k = cta_key[threadIdx.x] != 0ull ? cta_key[threadIdx.x] : 1ull;
@@ -38,14 +40,8 @@ __device__ __forceinline__ void finish_argmax(const GemvArgs& a, const unsigned 
     if (blockIdx.x != 0) return;
     __shared__ unsigned long long s_red[16];
     __shared__ int s_late;
-    __shared__ unsigned int s_dirty;
     if (threadIdx.x < 16) s_red[threadIdx.x] = 0ull;
-    if (threadIdx.x == 0) {
-        s_late = 0;
-        unsigned int d;
-        asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(d) : "l"(&a.ws->dirty) : "memory");
-        s_dirty = d;
-    }
+    if (threadIdx.x == 0) s_late = 0;
     __syncthreads();
     const int G = static_cast<int>(gridDim.x);
     for (int j = threadIdx.x; j < G * a.M; j += blockDim.x) {
@@ -58,8 +54,8 @@ __device__ __forceinline__ void finish_argmax(const GemvArgs& a, const unsigned 
     }
     // a dirty bank left by an earlier step (never this step's bank): zero the
     // slots that step used
-    if (s_dirty & 1u) {
-        const unsigned int db = (s_dirty >> 1) & 1u, dm = (s_dirty >> 2) & 31u, dg = s_dirty >> 8;
+    if (dirty & 1u) {
+        const unsigned int db = (dirty >> 1) & 1u, dm = (dirty >> 2) & 31u, dg = dirty >> 8;
         for (unsigned int j = threadIdx.x; j < dm * dg; j += blockDim.x)
             asm volatile("st.relaxed.gpu.global.u64 [%0], 0;" :: "l"(&a.ws->slots[db][j / dg][j % dg]) : "memory");
     }
@@ -70,7 +66,7 @@ __device__ __forceinline__ void finish_argmax(const GemvArgs& a, const unsigned 
             atomicOr(&a.ws->error, kDevErrTimeout);
             d = 1u | (bank << 1) | (static_cast<unsigned int>(a.M) << 2) | (static_cast<unsigned int>(G) << 8);
         }
-        if (s_late || (s_dirty & 1u)) a.ws->dirty = d;
+        if (s_late || (dirty & 1u)) a.ws->dirty = d;
         a.ws->epoch = epoch + 1u;
     }
     if (threadIdx.x < a.M) {

@@ -309,7 +309,7 @@ __global__ void __launch_bounds__(Cfg<FMT, K, MT>::THREADS, Cfg<FMT, K, MT>::MIN
     __shared__ unsigned long long s_best[NRED];
     __shared__ unsigned long long s_cta[MT];
     __shared__ int s_abort;
-    __shared__ unsigned int s_epoch;  // top-tokens mode: the workspace's epoch (slot bank)
+    __shared__ uint2 s_epoch;  // top-tokens mode: the workspace's epoch (slot bank) and dirty word
     __shared__ float s_amx[C::W8A8 ? NW : 1][16];  // W8A8: per compute warp and draft, max |h|
     // dh_idx of this CTA's first kIdCap tiles: [i][0..15] the rows' ids, [i][16]
     // the id of the row after the tile (copied when that row exists)
@@ -449,7 +449,7 @@ __global__ void __launch_bounds__(Cfg<FMT, K, MT>::THREADS, Cfg<FMT, K, MT>::MIN
         // best key per (row, draft), or writes the logits; never blocks the
         // compute warps except when it falls RS tiles behind.
         const int rl = (warp - NW) * 32 + lane;  // this reducer thread's first unit
-        if (!LOGITS && rl == 0) s_epoch = load_epoch(a.ws);  // the slot bank of the argmax hand-off
+        if (!LOGITS && rl == 0) s_epoch = load_epoch_dirty(a.ws);  // for the argmax hand-off
         cp_async_wait_all();  // this thread's dh_idx copies, then everyone's
         if constexpr (C::NRW > 1) named_bar_sync(1, 32 * C::NRW);
         else __syncwarp();
@@ -496,6 +496,17 @@ __global__ void __launch_bounds__(Cfg<FMT, K, MT>::THREADS, Cfg<FMT, K, MT>::MIN
                         acc[3] += q4.w;
                     }
                     v[0] = (acc[0] + acc[1]) + (acc[2] + acc[3]);
+                } else if constexpr (C::RED_T && NW % 2 == 0) {
+                    // two running sums of float2 reads, then their sum
+                    const float2* pr = reinterpret_cast<const float2*>(part(slot, 0, row_t, 0));
+                    float acc[2] = {0.0f, 0.0f};
+#pragma unroll
+                    for (int w2 = 0; w2 < NW / 2; ++w2) {
+                        const float2 q2 = pr[w2];
+                        acc[0] += q2.x;
+                        acc[1] += q2.y;
+                    }
+                    v[0] = acc[0] + acc[1];
                 } else
 #pragma unroll 4
                 for (int w = 0; w < NW; ++w) {
@@ -937,7 +948,7 @@ __global__ void __launch_bounds__(Cfg<FMT, K, MT>::THREADS, Cfg<FMT, K, MT>::MIN
             s_cta[tid] = k;
         }
         __syncthreads();
-        finish_argmax(a, s_cta, s_epoch);
+        finish_argmax(a, s_cta, s_epoch.x, s_epoch.y);
     }
 }
 
