@@ -44,13 +44,14 @@ FALLBACK_HBM_GBS = 6800.0
 # The method needs dh_idx only for the winning row; the kernel stages all of it
 # (256 KB, L2-resident from step to step) so that its argmax keys carry ids.
 N_ROWS, K_HID = 64_064, 2_560
+FLUSH_BYTES = 256 << 20                                   # 2 x the 129 MB L2
 STEP_BYTES = N_ROWS * (K_HID // 2) + N_ROWS * (K_HID // 16) + 4 + 2 * K_HID + 4
 
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum, mean of two
 # launches) of one launch of the M = 1 GEMV, from an ncu capture of
 # `bench.py --profile`; reported only while the kernel sources still hash to
 # kernel_sha (else null).
-TRAFFIC = {"kernel_sha": "94eb39504c1bb05c", "bytes_per_launch": 95_060_096}
+TRAFFIC = {"kernel_sha": "46359883ca9f01f6", "bytes_per_launch": 94_915_840}
 
 
 def kernel_sha() -> str:
@@ -318,6 +319,26 @@ def run_ours(args, world, rank, local):
         torch.distributed.barrier()
     assert head.device_error() == 0
 
+    # L2-flush cross-check: one head copy; before each step a 256 MB write
+    # (2 x L2) evicts the head from L2, and the step alone is timed with events
+    # around it. The flush sits between consecutive steps, so this leg has no
+    # overlap between steps (each one starts cold and ends before the next).
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    n_fl = min(K, 200)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_fl)]
+    with torch.cuda.stream(s):
+        for i in range(n_fl):
+            flush.fill_(i & 0xFF)
+            evs[i][0].record(s)
+            head.top_tokens(hs[Wm + i:Wm + i + 1], ids=ids[Wm + i])
+            evs[i][1].record(s)
+        s.synchronize()
+    fl_us = sorted(a.elapsed_time(b) * 1e3 for a, b in evs)
+    l2_flush = {"median_us_per_step": fl_us[len(fl_us) // 2], "mean_us_per_step": sum(fl_us) / len(fl_us),
+                "steps": n_fl, "flush_bytes": FLUSH_BYTES,
+                "how": "one head copy; a 256 MB write before each step; each step timed alone with CUDA events"}
+    del flush
+
     # End to end through the public call with host buffers
     # (draft_head_top_tokens_host): per step, one call copies the hidden state
     # from pinned host memory, runs the draft step and copies the id back.
@@ -400,6 +421,7 @@ def run_ours(args, world, rank, local):
           "cpu_baseline": cpu, "cpu_baseline_all_cores": cpu_all,
           "e2e": {"value": whole_job_us_per_step(ms_e2e, K, world), "unit": "us/step", "h2d_bytes_per_step": 2 * K_HID,
                   "d2h_bytes_per_step": 4, "ids_match_graph": e2e_ok, "call": "draft_head_top_tokens_host"},
+          "l2_flush_leg": l2_flush,
           "gpu_launches": K, "clocks": clocks, "parity": parity,
           "library": os.path.relpath(dh.library_path(), ROOT), "kernel_sha": sha})
     if world > 1:
