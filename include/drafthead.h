@@ -225,9 +225,13 @@ int draft_head_top_tokens(const dh_head_t *hd, const void *h, int M, int32_t *id
  * draft_head_top_tokens on it, and the copies of the ids (int32 [M]) and,
  * when top_host is not NULL, the top logits (fp32 [M]) back to ids_host /
  * top_host. It returns once they are enqueued; the host results are valid
- * after the stream synchronises. Page-locked host buffers keep the copies
- * asynchronous (pageable ones work, but the copies then wait on the calling
- * thread, and stream capture refuses them). The caller owns every buffer;
+ * after the stream synchronises. Page-locked host buffers that the device
+ * addresses directly (cudaHostAlloc, torch pin_memory(); h 16-byte aligned,
+ * ids and top 4-byte aligned) take a path without copy-engine transfers: a
+ * one-CTA kernel gathers h into the staging area and the draft step writes
+ * the ids (and top logits) into the host buffers. Other host buffers are
+ * copied with cudaMemcpyAsync (pageable ones work, but those copies wait on
+ * the calling thread, and stream capture refuses them). The caller owns every buffer;
  * ws must be draft_head_workspace_bytes(hd, M_max) bytes with M_max >= M and
  * initialised; calls that overlap on the GPU must not share a workspace.
  * Errors: as draft_head_top_tokens (no alignment rule on the host buffers),

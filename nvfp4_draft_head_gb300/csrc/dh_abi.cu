@@ -40,6 +40,17 @@ size_t round_up(size_t n, size_t a) { return (n + a - 1) / a * a; }
 size_t stage_h_bytes(int K, int M) { return round_up(static_cast<size_t>(M) * static_cast<size_t>(K) * 2, DH_WORKSPACE_ALIGN); }
 size_t stage_bytes(int K, int M) { return stage_h_bytes(K, M) + round_up(kStageIds, DH_WORKSPACE_ALIGN); }
 
+// True if p is page-locked host memory the device reads and writes at the
+// same address (unified addressing), e.g. from cudaHostAlloc / pin_memory().
+bool device_mapped(const void* p) {
+    cudaPointerAttributes at;
+    if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return false;
+    }
+    return at.type == cudaMemoryTypeHost && at.devicePointer == p;
+}
+
 int check_gather(const void* W, int V, int K, const int32_t* idx, int N) {
     if (W == nullptr || idx == nullptr) return DH_ERR_ARG;
     if (V <= 0 || K <= 0 || N <= 0) return DH_ERR_SHAPE;
@@ -242,9 +253,23 @@ int draft_head_top_tokens_host(const dh_head_t* hd, const void* h_host, int M, i
     if ((st = check_ws(ws, ws_bytes, sizeof(dh::Workspace) + stage_bytes(hd->K, M))) != DH_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     uint8_t* stage = static_cast<uint8_t*>(ws) + sizeof(dh::Workspace);
+    const size_t hbytes = static_cast<size_t>(M) * hd->K * 2;
+    // Page-locked buffers the device can address: a one-CTA kernel gathers h
+    // into the staging area and the draft step writes the ids (and top
+    // logits) straight into the host buffers; no copy-engine transfer sits
+    // between the kernels, so they keep their programmatic-launch overlap.
+    if (aligned(h_host, 16) && aligned(ids_host, 4) && (top_host == nullptr || aligned(top_host, 4)) &&
+        device_mapped(h_host) && device_mapped(ids_host) && (top_host == nullptr || device_mapped(top_host))) {
+        cudaError_t e = dh::launch_stage_rows(h_host, stage, hbytes, s);
+        if (e != cudaSuccess) return cuda_status(e);
+        dh::GemvArgs a = dh::step_args(hd, stage, M, ws);
+        a.ids = ids_host;
+        a.top = top_host;
+        return cuda_status(dh::launch_gemv(a, s));
+    }
     int32_t* ids = reinterpret_cast<int32_t*>(stage + stage_h_bytes(hd->K, M));
     float* top = reinterpret_cast<float*>(ids + DH_MAX_M);
-    cudaError_t e = cudaMemcpyAsync(stage, h_host, static_cast<size_t>(M) * hd->K * 2, cudaMemcpyHostToDevice, s);
+    cudaError_t e = cudaMemcpyAsync(stage, h_host, hbytes, cudaMemcpyHostToDevice, s);
     if (e != cudaSuccess) return cuda_status(e);
     dh::GemvArgs a = dh::step_args(hd, stage, M, ws);
     a.ids = ids;

@@ -44,6 +44,46 @@ cudaError_t launch_keys_to_ids(const unsigned long long* keys, int M, int32_t* i
     return cudaGetLastError();
 }
 
+// Hidden rows from page-locked host memory into the workspace staging area,
+// 16 bytes per thread (a draft step's rows: M x K x 2 <= 16 x 5120 x 2 bytes).
+// The loads are issued before the grid-dependency wait (the host wrote the
+// rows before the call), the stores after it.
+__global__ void __launch_bounds__(1024) stage_rows_kernel(const uint4* src, uint4* dst, int n16) {
+    constexpr int kPer = 10;  // 16-byte pieces per thread: 1024 x 10 x 16 = 160 KB
+    uint4 v[kPer];
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+        const int i = threadIdx.x + j * blockDim.x;
+        if (i < n16) v[j] = src[i];
+    }
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+        const int i = threadIdx.x + j * blockDim.x;
+        if (i < n16) dst[i] = v[j];
+    }
+    __syncthreads();
+    asm volatile("griddepcontrol.launch_dependents;");
+}
+
+cudaError_t launch_stage_rows(const void* src_host, void* dst, size_t bytes, cudaStream_t s) {
+    const int n16 = static_cast<int>(bytes / 16);
+    if (bytes % 16 != 0 || n16 > 1024 * 10) return cudaErrorInvalidValue;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(1);
+    cfg.blockDim = dim3(n16 < 1024 ? ((n16 + 31) / 32) * 32 : 1024);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, stage_rows_kernel, static_cast<const uint4*>(src_host),
+                                       static_cast<uint4*>(dst), n16);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
+
 // Self-test of the bounded waits: wait for an event that never happens (kind
 // 0: a workspace word nothing writes, polled like the argmax hand-off's slots;
 // kind 1: an mbarrier nothing arrives on, waited on like the pipeline's), give

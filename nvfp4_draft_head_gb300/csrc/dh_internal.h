@@ -48,6 +48,12 @@ cudaError_t launch_nvfp4_pack(const uint8_t* q, const uint8_t* sf, int N, int K,
 // and optional top logits. One single-warp kernel.
 cudaError_t launch_keys_to_ids(const unsigned long long* keys, int M, int32_t* ids, float* top, cudaStream_t s);
 
+// Copy `bytes` (a multiple of 16, both pointers 16-byte aligned) from
+// device-addressable host memory into a device buffer with one CTA: it reads
+// before the grid-dependency wait and writes after it (the draft step that
+// read the buffer last may still be running).
+cudaError_t launch_stage_rows(const void* src_host, void* dst, size_t bytes, cudaStream_t s);
+
 // Fill out[0..count) with -inf.
 cudaError_t launch_fill_neg_inf(float* out, size_t count, cudaStream_t s);
 
