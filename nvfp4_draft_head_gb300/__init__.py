@@ -116,9 +116,17 @@ def _ptr(t) -> int | None:
     return None if t is None else t.data_ptr()
 
 
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
 def _stream(stream=None) -> int:
-    s = torch.cuda.current_stream() if stream is None else stream
-    return s.cuda_stream
+    """cudaStream_t of `stream`, or of the current stream (without building a
+    Stream object: this runs once per draft step)."""
+    if stream is not None:
+        return stream.cuda_stream
+    if _raw_stream is not None:
+        return _raw_stream(torch.cuda.current_device())
+    return torch.cuda.current_stream().cuda_stream
 
 
 def _workspace(nbytes: int, device) -> torch.Tensor:
@@ -312,10 +320,11 @@ class DraftHead:
         M = self._check_h(h)
         if ids is None:
             ids = torch.empty(M, dtype=torch.int32, pin_memory=h.is_pinned())
-        for name, t, dt in (("ids", ids, torch.int32), ("top", top, torch.float32)):
-            if t is not None and (t.device.type != "cpu" or t.dtype != dt or t.numel() != M
-                                  or not t.is_contiguous()):
-                raise ValueError(f"{name} must be a contiguous CPU {dt} tensor of {M} elements")
+        elif ids.device.type != "cpu" or ids.dtype != torch.int32 or ids.numel() != M or not ids.is_contiguous():
+            raise ValueError(f"ids must be a contiguous CPU torch.int32 tensor of {M} elements")
+        if top is not None and (top.device.type != "cpu" or top.dtype != torch.float32 or top.numel() != M
+                                or not top.is_contiguous()):
+            raise ValueError(f"top must be a contiguous CPU torch.float32 tensor of {M} elements")
         _check("draft_head_top_tokens_host",
                lib().draft_head_top_tokens_host(C.byref(self.desc), h.data_ptr(), M, ids.data_ptr(),
                                                 _ptr(top), self.ws.data_ptr(), self.ws_bytes,
