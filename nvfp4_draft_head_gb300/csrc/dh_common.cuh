@@ -257,6 +257,89 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
     return p;
 }
 
+// ------------------------------------------------------------------------
+// Thread-block clusters of two CTAs: distributed shared memory between the
+// CTAs of a pair (the partner's address of a shared variable, stores to it,
+// arrivals on its mbarriers) and the cluster-wide barrier.
+// ------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t cluster_id_x() {
+    uint32_t r;
+    asm("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t cluster_count_x() {
+    uint32_t r;
+    asm("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
+    return r;
+}
+
+// The shared::cluster address of `p` (a variable of this CTA) in CTA `rank`.
+__device__ __forceinline__ uint32_t cluster_map(const void* p, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
+    return r;
+}
+
+__device__ __forceinline__ void st_cluster_f32(uint32_t addr, float x) {
+    asm volatile("st.shared::cluster.f32 [%0], %1;" :: "r"(addr), "f"(x) : "memory");
+}
+
+__device__ __forceinline__ void st_cluster_f32x2(uint32_t addr, float x, float y) {
+    asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" :: "r"(addr), "f"(x), "f"(y) : "memory");
+}
+
+// Arrive on an mbarrier of another CTA of the cluster (address from
+// cluster_map), releasing this thread's earlier writes at cluster scope.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t bar) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" :: "r"(bar) : "memory");
+}
+
+// Bounded wait on a local mbarrier that another CTA of the cluster arrives on
+// (acquire at cluster scope: its writes released by the arrivals are visible).
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, uint32_t limit = kWaitLimit) {
+    const uint32_t a = smem_u32(bar);
+    for (uint32_t i = 0; i < limit; ++i) {
+        uint32_t done;
+        asm volatile("{\n\t.reg .pred p;\n\t"
+                     "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
+                     "selp.u32 %0, 1, 0, p;\n\t}"
+                     : "=r"(done) : "r"(a), "r"(parity), "n"(kSuspendNs) : "memory");
+        if (done) return true;
+    }
+    return false;
+}
+
+// Every thread of every CTA of the cluster: a hardware barrier (no spin loop
+// of ours). The arrival is relaxed: it does not wait for this thread's loads
+// and stores in flight (a released arrival would hold the CTA until its tile
+// loads or its result stores have landed); a thread whose remote accesses
+// must be complete before the others pass calls cluster_fence() first.
+__device__ __forceinline__ void cluster_arrive() {
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void cluster_wait() {
+    asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void cluster_sync_all() {
+    cluster_arrive();
+    cluster_wait();
+}
+
+// This thread's earlier memory accesses, remote ones included, are performed
+// at cluster scope before its later ones.
+__device__ __forceinline__ void cluster_fence() {
+    asm volatile("fence.acq_rel.cluster;" ::: "memory");
+}
+
 // Named barrier among `threads` threads (id 1..15; id 0 is __syncthreads).
 __device__ __forceinline__ void named_bar_sync(int id, int threads) {
     asm volatile("bar.sync %0, %1;" :: "r"(id), "r"(threads) : "memory");

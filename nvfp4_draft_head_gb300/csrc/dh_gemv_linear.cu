@@ -22,7 +22,7 @@ cudaError_t launch_linear_nvfp4_packed_extra(const GemvArgs& a, cudaStream_t s) 
                 if (a.M <= 2) return mma::launch_mma<mma::kFmtPackedRing, 4096, 2, true>(a, s);
                 return mma::launch_mma<mma::kFmtPackedRing, 4096, 4, true>(a, s);
             }
-            return mma::launch_mma_m<mma::kFmtPackedLdg, 4096, true>(a, s);
+            return mma::launch_mma_m_wide<mma::kFmtPackedLdg, 4096, true>(a, s);
         default: return cudaErrorInvalidValue;
     }
 }

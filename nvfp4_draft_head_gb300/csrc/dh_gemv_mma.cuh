@@ -102,8 +102,20 @@ struct Cfg {
     // µs top tokens, 19.8 -> 18.4 compute_logits; at 4 drafts and more the
     // 80-register cap of two CTAs per SM spills.
     static constexpr bool TWO_CTA = FMT == kFmtPackedRing && MT <= 2 && NWIN == 20;
-    static constexpr int NW = largest_divisor_at_most(NWIN, TWO_CTA ? 10 : kMaxComputeWarps);  // compute warps
-    static constexpr int WPW = NWIN / NW;                    // windows per warp
+    // Register-load kernels with more windows than compute warps (K = 4,096
+    // and 5,120; the packed head at 8 and 16 drafts, fewer take the ring): the
+    // K range is split over the two CTAs of a cluster, each with one window
+    // per warp; the second CTA's reducer sends its sums into the first CTA's
+    // shared memory (distributed shared memory), which writes the results.
+    // Each SM reads half of h, whose replicated reads (all of h by every CTA,
+    // 160 KB at K = 5,120 and 16 drafts) bounded these kernels, and no warp
+    // holds two windows' h fragments (which spilled at 80 registers).
+    static constexpr int KS =
+        (FMT != kFmtPackedRing && NWIN > kMaxComputeWarps && (FMT != kFmtPackedLdg || MT >= 8)) ? 2 : 1;
+    static constexpr int NWC = NWIN / KS;                    // windows of one CTA
+    static constexpr int XS = 4;                             // exchange slots of a pair
+    static constexpr int NW = largest_divisor_at_most(NWC, TWO_CTA ? 10 : kMaxComputeWarps);  // compute warps
+    static constexpr int WPW = NWC / NW;                     // windows per warp
     static constexpr int MINB = TWO_CTA ? 2 : 1;             // CTAs per SM the registers must allow
     static constexpr int NT = MT <= 8 ? 1 : 2;               // n8 tiles of drafts
     // suspend-time hint on pipeline waits: register-load kernels at one and
@@ -129,7 +141,7 @@ struct Cfg {
     // µs per step. Slower at 2 drafts (+0.5 µs) and at 16 (+2.3 µs with two
     // tiles in flight; spills with three). Packed layout only: the canonical
     // layout's scale ring owns the dynamic shared memory.
-    static constexpr bool SMB = PACKED && !BLOCKDIAG && WPW == 1 && (MT == 4 || MT == 8);
+    static constexpr bool SMB = !BLOCKDIAG && ((PACKED && WPW == 1 && (MT == 4 || MT == 8)) || (FMT == 3 && MT >= 16));
     // Register-load kernels: tiles of loads in flight in registers, as many as
     // fit next to the h fragments (16 registers per window and n8 tile) in the
     // 80 registers that 21+ warps per SM allow, up to a cap: three with one n8
@@ -140,7 +152,7 @@ struct Cfg {
     // µs against three), four at two and eight drafts (21.43 -> 20.99, 22.19 ->
     // 21.55; four at four drafts was slower), two at 16 (three spilled).
     static constexpr int PCAP = PACKED ? (MT == 1 ? 2 : (MT == 2 ? 4 : (MT >= 16 ? 2 : 3)))
-                                       : ((MT >= 16 || FMT == 2 || FMT == 5) ? 2 : 3);
+                                       : (MT >= 16 ? 1 : ((FMT == 2 || FMT == 5) ? 2 : 3));
     // Packed layout: the head streams through a ring of whole tiles in shared
     // memory, filled by one producer thread with 1-D bulk copies (the tiles of
     // this layout are contiguous). Its first RPRE tiles are issued before the
@@ -155,8 +167,8 @@ struct Cfg {
     static constexpr int TB = NWIN * WBLK;                    // packed: bytes of one tile
     static constexpr int RPRE = TWO_CTA ? 1 : 4;
     static constexpr int P = RING ? ((WPW == 1 && MT <= 8) ? 2 : 1)
-                                  : (SMB ? (MT == 8 ? 4 : 3)
-                                         : cmax(1, cmin(PCAP, (kLoadRegBudget - WPW * NT * 16) / TILE_REGS)));
+                                  : ((SMB && PACKED) ? (MT == 8 ? 4 : 3)
+                                         : cmax(1, cmin(PCAP, (kLoadRegBudget - (SMB ? 0 : WPW * NT * 16)) / TILE_REGS)));
     // Canonical NVFP4 layout: a loader warp streams each tile's scale bytes
     // into a shared-memory ring with 1-D bulk copies.
     static constexpr bool SCALES = (FMT == 1);
@@ -181,16 +193,22 @@ struct Cfg {
     static constexpr int RS = RING ? cclamp(PART_BUDGET / PART_SLOT, 2, 16)
                                    : ((PACKED && MT == 1) ? 8 : ((4 * NW * 16 * MT * 4 <= 40 * 1024) ? 4 : 2));
     static constexpr int PART_DYN = RING ? RS * PART_SLOT : 0;
-    static constexpr int SMB_BYTES = SMB ? NW * NT * 8 * 32 * 8 : 0;
+    static constexpr int SMB_BYTES = SMB ? NW * WPW * NT * 8 * 32 * 8 : 0;
     // packed layout: dynamic shared memory of a CTA (one or two per SM) and
     // the tiles of its ring, as many as fit next to the partials and the h
     // fragments, 2 to 8
     static constexpr int RING_BUDGET = TWO_CTA ? 96 * 1024 : 200 * 1024;
     static constexpr int RT = RING ? cclamp((RING_BUDGET - PART_DYN - SMB_BYTES) / TB, 2, 8) : 0;
     static constexpr int NSB = RING ? RT : SS;                         // tile / scale ring barriers
+    // K split: the exchange area after the scale ring or the h fragments:
+    // the sums' slots, their full and empty barriers, and (W8A8) the
+    // partner's max |h| per draft with its barrier
+    static constexpr int XOFF = LOADER ? SS * SLOT : SMB_BYTES;
+    static constexpr int XB_BYTES = KS == 2 ? XS * 16 * MT * 4 + 2 * XS * 8 + 16 * 4 + 8 : 0;
     static constexpr size_t DYN_SMEM = RING ? static_cast<size_t>(RT) * TB + PART_DYN + SMB_BYTES
-                                            : (LOADER ? static_cast<size_t>(SS) * SLOT : static_cast<size_t>(SMB_BYTES));
-    static_assert(NWIN % NW == 0, "windows must split evenly over warps");
+                                            : static_cast<size_t>(XOFF + XB_BYTES);
+    static_assert(!(KS == 2 && RING), "the K split is for the register-load kernels");
+    static_assert(NWIN % KS == 0 && NWC % NW == 0, "windows must split evenly over CTAs and warps");
     static_assert(K % 128 == 0, "K must be a multiple of 128");
 };
 
@@ -239,12 +257,12 @@ struct TileBuf {
 };
 
 template <int FMT, int K, int MT>
-__device__ __forceinline__ void load_tile(TileBuf<FMT, K, MT>& b, const uint8_t* q, int tile, int warp, int g,
+__device__ __forceinline__ void load_tile(TileBuf<FMT, K, MT>& b, const uint8_t* q, int tile, int wbase, int g,
                                           int t) {
     using C = Cfg<FMT, K, MT>;
 #pragma unroll
     for (int ww = 0; ww < C::WPW; ++ww) {
-        const int w = warp + ww * C::NW;
+        const int w = wbase + ww * C::NW;  // window
         if constexpr (C::PACKED) {
             // block (tile, w): 16 rows x 64 code bytes, then 4 scale bytes per lane
             const uint8_t* blk = q + (static_cast<size_t>(tile) * C::NWIN + w) * C::WBLK;
@@ -314,12 +332,29 @@ __global__ void __launch_bounds__(Cfg<FMT, K, MT>::THREADS, Cfg<FMT, K, MT>::MIN
     // dh_idx of this CTA's first kIdCap tiles: [i][0..15] the rows' ids, [i][16]
     // the id of the row after the tile (copied when that row exists)
     __shared__ __align__(16) int s_ids[kIdCap * 20];
+    // K split over a pair (dynamic shared memory): the second CTA's per-tile
+    // sums [slot][row][draft] in the first CTA, which waits on xfull[slot];
+    // the second waits on xempty[slot] until the first has read a slot
+    float* const s_xb = reinterpret_cast<float*>(s_dyn + C::XOFF);
+    uint64_t* const xfull = reinterpret_cast<uint64_t*>(s_dyn + C::XOFF + C::XS * NRED * 4);
+    uint64_t* const xempty = xfull + C::XS;
+    float* const amx_rx = reinterpret_cast<float*>(xempty + C::XS);  // W8A8: the partner's max |h| per draft
+    uint64_t* const amx_bar = reinterpret_cast<uint64_t*>(amx_rx + 16);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int g = lane >> 2, t = lane & 3;
     const int n_tiles = a.N / 16;
-    const int b0 = static_cast<int>(blockIdx.x);
-    const int my_tiles = b0 < n_tiles ? (n_tiles - 1 - b0) / static_cast<int>(gridDim.x) + 1 : 0;
-    auto tile_of = [&](int i) { return b0 + i * static_cast<int>(gridDim.x); };
+    // tiles go to CTAs, or with the K split to pairs (clusters of two)
+    const int crank = C::KS == 2 ? static_cast<int>(cluster_ctarank()) : 0;
+    const int b0 = C::KS == 2 ? static_cast<int>(cluster_id_x()) : static_cast<int>(blockIdx.x);
+    // (read where used, not held in a register)
+    auto n_units = [&]() -> int {
+        if constexpr (C::KS == 2) return static_cast<int>(cluster_count_x());
+        else return static_cast<int>(gridDim.x);
+    };
+    const int my_tiles = b0 < n_tiles ? (n_tiles - 1 - b0) / n_units() + 1 : 0;
+    auto tile_of = [&](int i) { return b0 + i * n_units(); };
+    const int wbase = crank * C::NWC + warp;  // a compute warp's first window
+    const bool xsend = C::KS == 2 && crank == 1;  // sends its sums instead of writing results
     const uint8_t* q = static_cast<const uint8_t*>(a.q);
     volatile int* abort_flag = &s_abort;
     // Wait for a pipeline barrier phase. The first test does not block and
@@ -341,7 +376,7 @@ __global__ void __launch_bounds__(Cfg<FMT, K, MT>::THREADS, Cfg<FMT, K, MT>::MIN
     if (!C::RING && warp < NW) {
 #pragma unroll
         for (int p = 0; p < P; ++p)
-            if (p < my_tiles) load_tile<FMT, K, MT>(buf[p], q, tile_of(p), warp, g, t);
+            if (p < my_tiles) load_tile<FMT, K, MT>(buf[p], q, tile_of(p), wbase, g, t);
     }
 
     if (tid == 0) {
@@ -353,10 +388,21 @@ __global__ void __launch_bounds__(Cfg<FMT, K, MT>::THREADS, Cfg<FMT, K, MT>::MIN
             mbar_init(&full_s[r], 1);
             mbar_init(&empty_s[r], NW);
         }
+        if constexpr (C::KS == 2) {
+            for (int r = 0; r < C::XS; ++r) {
+                mbar_init(&xfull[r], 32 * C::NRW);
+                mbar_init(&xempty[r], 32 * C::NRW);
+            }
+            mbar_init(amx_bar, 16);
+        }
         s_abort = 0;
         mbar_init_fence();
     }
     __syncthreads();  // barriers initialised
+    // K split: the partner's barriers are initialised before either CTA reaches
+    // into the other's shared memory; every thread arrives here and waits
+    // before its first access to the partner (reducer) or at the end
+    if constexpr (C::KS == 2) cluster_arrive();
     // The loader's copies of ring slot i % SS (tile i of this CTA).
     const uint64_t pol = policy_evict_first();
     auto issue = [&](int i) {
@@ -384,7 +430,7 @@ __global__ void __launch_bounds__(Cfg<FMT, K, MT>::THREADS, Cfg<FMT, K, MT>::MIN
     // The reducer warps start copying dh_idx for their tiles now: it belongs to
     // the head, so the copies overlap the preceding kernel's tail instead of
     // sitting on the reducer's path once the partials arrive.
-    const int n_pre = ((LOGITS || a.idx_ascending) && a.idx != nullptr &&
+    const int n_pre = (!xsend && (LOGITS || a.idx_ascending) && a.idx != nullptr &&
                        (reinterpret_cast<uintptr_t>(a.idx) & 15u) == 0)
                           ? (my_tiles < kIdCap ? my_tiles : kIdCap)
                           : 0;
@@ -459,6 +505,57 @@ __global__ void __launch_bounds__(Cfg<FMT, K, MT>::THREADS, Cfg<FMT, K, MT>::MIN
         constexpr int UPR = MT / DV;                                    // units per row
         constexpr int NU = 16 * UPR;                                     // units per tile
         constexpr int SLOTS = (NU + 32 * C::NRW - 1) / (32 * C::NRW);  // units per reducer thread
+        static_assert(C::KS == 1 || NU <= 32 * C::NRW, "K split: at most one unit per reducer thread");
+        // the logit of (tile row row_t, draft m0 + d), written or kept as a key
+        auto emit = [&](int r0, int row_t, int m0, const float (&v)[DV], int id) {
+            const int row = r0 + row_t;
+            if (row >= a.n_kept) return;
+#pragma unroll
+            for (int d = 0; d < DV; ++d) {
+                const int m = m0 + d;
+                if (m >= a.M) break;
+                if constexpr (LOGITS) {
+                    // an id outside [0, V) is reported, not written
+                    if (id >= 0 && id < a.V) a.out[static_cast<size_t>(m) * a.V + id] = v[d] * gmul;
+                    else atomicOr(&a.ws->error, kDevErrIdx);
+                } else {
+                    // tie-break on the lower id (ascending dh_idx) or the lower row
+                    const unsigned long long key = argmax_key(ordered_key(v[d] * gmul), static_cast<uint32_t>(id));
+                    const int r = row_t * MT + m;
+                    if (key > s_best[r]) s_best[r] = key;
+                }
+            }
+        };
+        // K split: wait for a barrier the partner arrives on (a CTA whose
+        // waits already ran out stops waiting)
+        auto xwait = [&](uint64_t* bar, uint32_t parity) {
+            if (*abort_flag) return;
+            if (!mbar_wait_cluster(bar, parity)) {
+                atomicOr(&a.ws->error, kDevErrTimeout);
+                *abort_flag = 1;
+            }
+        };
+        // K split, first CTA: tile j's own sums wait in registers until the
+        // next tile's partials are in; then the partner's sums of tile j (in
+        // flight meanwhile) are added and the results written. Every reducer
+        // thread waits and arrives; those with a unit (rl < NU) also read and
+        // write.
+        float vprev[DV];
+#pragma unroll
+        for (int d = 0; d < DV; ++d) vprev[d] = 0.0f;
+        int idprev = 0, r0prev = 0;
+        auto finish_prev = [&](int j) {
+            const int xj = j % C::XS;
+            xwait(&xfull[xj], (j / C::XS) & 1);
+            if (rl < NU) {
+                float v[DV];
+#pragma unroll
+                for (int d = 0; d < DV; ++d) v[d] = vprev[d] + s_xb[xj * NRED + rl * DV + d];
+                emit(r0prev, rl / UPR, (rl % UPR) * DV, v, idprev);
+            }
+            if (j + C::XS < my_tiles) mbar_arrive_remote(cluster_map(&xempty[xj], 1));
+        };
+        if constexpr (C::KS == 2) cluster_wait();
         for (int i = 0; i < my_tiles; ++i) {
             const int slot = i % RS;
             const int tile = tile_of(i);
@@ -468,11 +565,19 @@ __global__ void __launch_bounds__(Cfg<FMT, K, MT>::THREADS, Cfg<FMT, K, MT>::MIN
             for (int k = 0; k < SLOTS; ++k) {
                 const int u = rl + k * 32 * C::NRW;
                 const int row = tile * 16 + u / UPR;
-                ids_[k] = ((LOGITS || a.idx_ascending) && u < NU && row < a.n_kept)
+                ids_[k] = (!xsend && (LOGITS || a.idx_ascending) && u < NU && row < a.n_kept)
                               ? (i < n_pre ? s_ids[20 * i + u / UPR] : (a.idx ? __ldg(a.idx + row) : row))
                               : row;
             }
             pipe_wait(&full_p[slot], (i / RS) & 1);
+            const int xi = i % C::XS;
+            if constexpr (C::KS == 2) {
+                if (xsend) {
+                    if (i >= C::XS) xwait(&xempty[xi], ((i / C::XS) - 1) & 1);  // the exchange slot is free
+                } else if (i > 0) {
+                    finish_prev(i - 1);
+                }
+            }
             const int r0 = tile * 16;
 #pragma unroll
             for (int k = 0; k < SLOTS; ++k) {
@@ -524,29 +629,36 @@ __global__ void __launch_bounds__(Cfg<FMT, K, MT>::THREADS, Cfg<FMT, K, MT>::MIN
                         v[0] += *part(slot, w, row_t, m0);
                     }
                 }
-                const int row = r0 + row_t;
-                if (row >= a.n_kept) continue;
-#pragma unroll
-                for (int d = 0; d < DV; ++d) {
-                    const int m = m0 + d;
-                    if (m >= a.M) break;
-                    if constexpr (LOGITS) {
-                        // an id outside [0, V) is reported, not written
-                        const int id = ids_[k];
-                        if (id >= 0 && id < a.V) a.out[static_cast<size_t>(m) * a.V + id] = v[d] * gmul;
-                        else atomicOr(&a.ws->error, kDevErrIdx);
+                if constexpr (C::KS == 2) {
+                    // this CTA's half of the K range: sent to the partner, or
+                    // held until the partner's half of this tile is added
+                    if (xsend) {
+                        const uint32_t ra = cluster_map(&s_xb[xi * NRED + u * DV], 0);
+                        if constexpr (DV == 2) st_cluster_f32x2(ra, v[0], v[1]);
+                        else st_cluster_f32(ra, v[0]);
                     } else {
-                        // tie-break on the lower id (ascending dh_idx) or the lower row
-                        const unsigned long long key =
-                            argmax_key(ordered_key(v[d] * gmul), static_cast<uint32_t>(ids_[k]));
-                        const int r = row_t * MT + m;
-                        if (key > s_best[r]) s_best[r] = key;
+#pragma unroll
+                        for (int d = 0; d < DV; ++d) vprev[d] = v[d];
+                        idprev = ids_[k];
                     }
+                } else {
+                    emit(r0, row_t, m0, v, ids_[k]);
                 }
+            }
+            if constexpr (C::KS == 2) {
+                if (xsend) mbar_arrive_remote(cluster_map(&xfull[xi], 0));
+                else r0prev = r0;
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty_p[slot]);
         }
+        if constexpr (C::KS == 2) {
+            if (!xsend && my_tiles > 0) finish_prev(my_tiles - 1);
+        }
+        // K split: this thread's stores into the partner's shared memory and
+        // arrivals on its barriers are complete before it passes the final
+        // cluster barrier (the partner then exits)
+        if constexpr (C::KS == 2) cluster_fence();
     } else {
         // -------------------------------------------------- compute warps ----
         // This thread's h words (B fragments), per window and n8 tile: word j
@@ -568,7 +680,7 @@ __global__ void __launch_bounds__(Cfg<FMT, K, MT>::THREADS, Cfg<FMT, K, MT>::MIN
                 float am = 0.0f;
 #pragma unroll
                 for (int ww = 0; ww < WPW; ++ww) {
-                    const int k0 = 128 * (warp + ww * NW) + 32 * t;
+                    const int k0 = 128 * (wbase + ww * NW) + 32 * t;
                     // the max |h| of this thread's 32 values (16-byte loads; the codes
                     // are made from a second read below): W8A8 4 drafts 42.3 -> 41.2 µs,
                     // 16 drafts 53.4 -> 50.6 µs against 4-byte loads
@@ -586,12 +698,29 @@ __global__ void __launch_bounds__(Cfg<FMT, K, MT>::THREADS, Cfg<FMT, K, MT>::MIN
                 if (t == 0) s_amx[warp][d] = am;
             }
             named_bar_sync(2, NW * 32);  // compute warps only
+            if constexpr (C::KS == 2) {
+                // the per-token scale takes the max over the whole K range: each
+                // CTA of the pair sends its max per draft to the other
+                cluster_wait();  // the partner's barriers are initialised
+                if (warp == 0 && lane < 16) {
+                    float am = 0.0f;
+                    for (int w2 = 0; w2 < NW; ++w2) am = fmaxf(am, s_amx[w2][lane]);
+                    st_cluster_f32(cluster_map(&amx_rx[lane], crank ^ 1), am);
+                    mbar_arrive_remote(cluster_map(amx_bar, crank ^ 1));
+                    cluster_fence();
+                }
+                if (!*abort_flag && !mbar_wait_cluster(amx_bar, 0)) {
+                    atomicOr(&a.ws->error, kDevErrTimeout);
+                    *abort_flag = 1;
+                }
+            }
             float sx_own[NT];  // scale of this lane's draft g + 8 nt
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
                 const int d = g + 8 * nt;
                 float am = 0.0f;
                 for (int w2 = 0; w2 < NW; ++w2) am = fmaxf(am, s_amx[w2][d]);
+                if constexpr (C::KS == 2) am = fmaxf(am, amx_rx[d]);
                 sx_own[nt] = act_fp8_scale(am);
                 unscale[nt][0] = __shfl_sync(0xFFFFFFFFu, sx_own[nt], 4 * (2 * t));
                 unscale[nt][1] = __shfl_sync(0xFFFFFFFFu, sx_own[nt], 4 * (2 * t + 1));
@@ -610,7 +739,7 @@ __global__ void __launch_bounds__(Cfg<FMT, K, MT>::THREADS, Cfg<FMT, K, MT>::MIN
                 const float sx = __shfl_sync(0xFFFFFFFFu, sx_own[d / 8], 4 * (d % 8));
 #pragma unroll
                 for (int ww = 0; ww < WPW; ++ww) {
-                    const int kw = (128 * (warp + ww * NW) + 4 * lane) / 2;  // u32 index of the lane's 4 values
+                    const int kw = (128 * (wbase + ww * NW) + 4 * lane) / 2;  // u32 index of the lane's 4 values
                     const uint2 v2 = __ldg(reinterpret_cast<const uint2*>(h32 + d * KW + kw));
                     const uint32_t w0 = v2.x, w1 = v2.y;
                     const uint32_t word = act_fp8_pair(w0, sx) | (act_fp8_pair(w1, sx) << 16);
@@ -622,6 +751,8 @@ __global__ void __launch_bounds__(Cfg<FMT, K, MT>::THREADS, Cfg<FMT, K, MT>::MIN
                 }
             }
         }
+        uint2* s_hb = reinterpret_cast<uint2*>(s_dyn + (C::RING ? static_cast<size_t>(C::RT) * C::TB + C::PART_DYN : 0)) +
+                      (C::SMB ? warp * WPW * NT * 8 * 32 : 0);  // [ww][nt][i][lane]
 #pragma unroll
         for (int nt = 0; nt < (C::W8A8 ? 0 : NT); ++nt) {
             const int d = C::BLOCKDIAG ? 0 : g + 8 * nt;
@@ -629,7 +760,7 @@ __global__ void __launch_bounds__(Cfg<FMT, K, MT>::THREADS, Cfg<FMT, K, MT>::MIN
             float am = 0.0f;
 #pragma unroll
             for (int ww = 0; ww < WPW; ++ww) {
-                const int k0 = 128 * (warp + ww * NW) + 32 * t;
+                const int k0 = 128 * (wbase + ww * NW) + 32 * t;
                 if constexpr (!(MT == 1 && LOGITS)) {
                 // 64 bytes of h per thread and window as four 16-byte loads (16 drafts:
                 // 32.2 -> 28.5 µs per step, 4 drafts -0.3 µs; the one-draft
@@ -678,6 +809,14 @@ __global__ void __launch_bounds__(Cfg<FMT, K, MT>::THREADS, Cfg<FMT, K, MT>::MIN
                         hb[ww][nt][j] = *reinterpret_cast<uint32_t*>(&v);
                     }
             }
+            if constexpr (C::SMB) {
+                // to shared memory as soon as they are made
+#pragma unroll
+                for (int ww = 0; ww < WPW; ++ww)
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        s_hb[((ww * NT + nt) * 8 + i) * 32 + lane] = make_uint2(hb[ww][nt][2 * i], hb[ww][nt][2 * i + 1]);
+            }
             if constexpr (C::BLOCKDIAG) {
                 unscale[nt][0] = inv;
                 unscale[nt][1] = inv;
@@ -698,15 +837,7 @@ __global__ void __launch_bounds__(Cfg<FMT, K, MT>::THREADS, Cfg<FMT, K, MT>::MIN
                 unscale[nt][1] = __shfl_sync(0xFFFFFFFFu, inv, 4 * (2 * t + 1));
             }
         }
-        uint2* s_hb = reinterpret_cast<uint2*>(s_dyn + (C::RING ? static_cast<size_t>(C::RT) * C::TB + C::PART_DYN : 0)) +
-                      (C::SMB ? warp * NT * 8 * 32 : 0);  // [nt][i][lane]
-        if constexpr (C::SMB) {
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-                for (int i = 0; i < 8; ++i) s_hb[(nt * 8 + i) * 32 + lane] = make_uint2(hb[0][nt][2 * i], hb[0][nt][2 * i + 1]);
-            __syncwarp();
-        }
+        if constexpr (C::SMB) __syncwarp();
         // Tile i's codes and scales into registers: from the ring (packed
         // layout: wait until the tile has landed, read this warp's windows,
         // free the slot) or with global loads.
@@ -717,7 +848,7 @@ __global__ void __launch_bounds__(Cfg<FMT, K, MT>::THREADS, Cfg<FMT, K, MT>::MIN
                 const uint8_t* tl = s_dyn + static_cast<size_t>(rs) * C::TB;
 #pragma unroll
                 for (int ww = 0; ww < WPW; ++ww) {
-                    const uint8_t* blk = tl + (warp + ww * NW) * C::WBLK;
+                    const uint8_t* blk = tl + (wbase + ww * NW) * C::WBLK;
                     b.c[ww][0][0] = *reinterpret_cast<const uint4*>(blk + g * 64 + 16 * t);
                     b.c[ww][1][0] = *reinterpret_cast<const uint4*>(blk + (g + 8) * 64 + 16 * t);
                     b.sp[ww] = *reinterpret_cast<const uint32_t*>(blk + 16 * 64 + 4 * lane);
@@ -725,7 +856,7 @@ __global__ void __launch_bounds__(Cfg<FMT, K, MT>::THREADS, Cfg<FMT, K, MT>::MIN
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&empty_s[rs]);
             } else {
-                load_tile<FMT, K, MT>(b, q, tile_of(i), warp, g, t);
+                load_tile<FMT, K, MT>(b, q, tile_of(i), wbase, g, t);
             }
         };
         if constexpr (C::RING) {
@@ -776,7 +907,7 @@ __global__ void __launch_bounds__(Cfg<FMT, K, MT>::THREADS, Cfg<FMT, K, MT>::MIN
                     const uint8_t* st = s_dyn + ss * C::SLOT;
 #pragma unroll
                     for (int ww = 0; ww < WPW; ++ww) {
-                        const int w = warp + ww * NW;
+                        const int w = wbase + ww * NW;
                         b.s[ww][0] = *reinterpret_cast<const uint2*>(st + g * C::SFB + 8 * w);
                         b.s[ww][1] = *reinterpret_cast<const uint2*>(st + (g + 8) * C::SFB + 8 * w);
                     }
@@ -916,11 +1047,16 @@ __global__ void __launch_bounds__(Cfg<FMT, K, MT>::THREADS, Cfg<FMT, K, MT>::MIN
                                 }
 #pragma unroll
                                 for (int nt = 0; nt < NT; ++nt) {
-                                    if constexpr (FMT == 3)
-                                        mma_bf16(out[nt], a0, a1, a2, a3, hb[ww][nt][2 * i], hb[ww][nt][2 * i + 1]);
-                                    else
+                                    if constexpr (FMT == 3) {
                                         if constexpr (C::SMB) {
-                                            const uint2 bb = s_hb[(nt * 8 + i) * 32 + lane];
+                                            const uint2 bb = s_hb[((ww * NT + nt) * 8 + i) * 32 + lane];
+                                            mma_bf16(out[nt], a0, a1, a2, a3, bb.x, bb.y);
+                                        } else {
+                                            mma_bf16(out[nt], a0, a1, a2, a3, hb[ww][nt][2 * i], hb[ww][nt][2 * i + 1]);
+                                        }
+                                    } else
+                                        if constexpr (C::SMB) {
+                                            const uint2 bb = s_hb[((ww * NT + nt) * 8 + i) * 32 + lane];
                                             mma_f16(out[nt], a0, a1, a2, a3, bb.x, bb.y);
                                         } else {
                                             mma_f16(out[nt], a0, a1, a2, a3, hb[ww][nt][2 * i], hb[ww][nt][2 * i + 1]);
@@ -937,7 +1073,16 @@ __global__ void __launch_bounds__(Cfg<FMT, K, MT>::THREADS, Cfg<FMT, K, MT>::MIN
             }
         }
     }
-    __syncthreads();
+    // with the K split, neither CTA of a pair exits while the other may still
+    // reach into its shared memory
+    __syncwarp();
+    if constexpr (C::KS == 2) {
+        // compute warps: the wait of the arrival at the start (W8A8: made in the prologue)
+        if (!C::W8A8 && warp < NW) cluster_wait();
+        cluster_sync_all();
+    } else {
+        __syncthreads();
+    }
     if constexpr (!LOGITS) {
         if (tid < MT) {
             unsigned long long k = 0ull;
@@ -966,31 +1111,44 @@ inline cudaError_t launch_mma(const GemvArgs& a, cudaStream_t s) {
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    int per_sm = occ[dev].load(std::memory_order_relaxed);
-    if (per_sm == 0) {
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-        if (e != cudaSuccess) return e;
-        int o = 0;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, kern, C::THREADS, smem);
-        if (e != cudaSuccess) return e;
-        per_sm = o > 0 ? o : 1;
-        occ[dev].store(per_sm, std::memory_order_relaxed);
-    }
-    const int n_tiles = a.N / 16;
-    int blocks = sms * per_sm;
-    if (blocks > n_tiles) blocks = n_tiles;
-    if (blocks > (n_tiles + C::MIN_TILES - 1) / C::MIN_TILES) blocks = (n_tiles + C::MIN_TILES - 1) / C::MIN_TILES;
-    if (blocks > kMaxGrid) blocks = kMaxGrid;  // one argmax slot per CTA
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(blocks);
+    cfg.gridDim = dim3(C::KS);
     cfg.blockDim = dim3(C::THREADS);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = C::KS;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = C::KS == 2 ? 2 : 1;
+    // resident CTAs: per SM x SMs, or with the K split 2 x the pairs that fit
+    int resident = occ[dev].load(std::memory_order_relaxed);
+    if (resident == 0) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+        if (e != cudaSuccess) return e;
+        int o = 0;
+        if constexpr (C::KS == 2) {
+            e = cudaOccupancyMaxActiveClusters(&o, kern, &cfg);
+            if (e != cudaSuccess) return e;
+            if (o <= 0) return cudaErrorInvalidConfiguration;
+            resident = C::KS * o;
+        } else {
+            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, kern, C::THREADS, smem);
+            if (e != cudaSuccess) return e;
+            resident = sms * (o > 0 ? o : 1);
+        }
+        occ[dev].store(resident, std::memory_order_relaxed);
+    }
+    const int n_tiles = a.N / 16;
+    int units = resident / C::KS;  // CTAs, or pairs
+    if (units > n_tiles) units = n_tiles;
+    if (units > (n_tiles + C::MIN_TILES - 1) / C::MIN_TILES) units = (n_tiles + C::MIN_TILES - 1) / C::MIN_TILES;
+    if (units * C::KS > kMaxGrid) units = kMaxGrid / C::KS;  // one argmax slot per CTA
+    cfg.gridDim = dim3(units * C::KS);
     e = cudaLaunchKernelEx(&cfg, kern, a);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
@@ -1001,6 +1159,15 @@ inline cudaError_t launch_mma_m(const GemvArgs& a, cudaStream_t s) {
     if (a.M <= 1) return launch_mma<FMT, K, 1, LOGITS>(a, s);
     if (a.M <= 2) return launch_mma<FMT, K, 2, LOGITS>(a, s);
     if (a.M <= 4) return launch_mma<FMT, K, 4, LOGITS>(a, s);
+    if (a.M <= 8) return launch_mma<FMT, K, 8, LOGITS>(a, s);
+    return launch_mma<FMT, K, 16, LOGITS>(a, s);
+}
+
+// Register-load kernels for 5 to 16 drafts only, at the widths where the ring
+// kernels take every launch of up to 4 drafts (packed_use_ring).
+template <int FMT, int K, bool LOGITS>
+inline cudaError_t launch_mma_m_wide(const GemvArgs& a, cudaStream_t s) {
+    if (a.M <= 4) return cudaErrorInvalidValue;
     if (a.M <= 8) return launch_mma<FMT, K, 8, LOGITS>(a, s);
     return launch_mma<FMT, K, 16, LOGITS>(a, s);
 }

@@ -276,6 +276,67 @@ def test_nvfp4_linear(N, K):
         check_logits(y, y_o, A, f"linear N={N} K={K} M={M}")
 
 
+@pytest.mark.parametrize("K", [4096, 5120])
+def test_k_split_over_cta_pairs(K):
+    """5 to 16 drafts at K = 4,096 / 5,120, where each tile's K range is split
+    over the two CTAs of a cluster: 388 tiles, so a pair takes more tiles than
+    it has exchange slots, and the last round of tiles is ragged. At K = 5,120
+    also a packed head in top-tokens mode (only the first CTA of a pair holds
+    argmax keys)."""
+    N = 6208
+    W = syn.head_bf16(4200 + K, N, K)
+    lin = dh.NVFP4Linear(dev_bf16(W))
+    q_o, sf_o, g_o = oracle.nvfp4_quantize(W, np.arange(N, dtype=np.int32))
+    for M in (6, 8, 16):
+        x = syn.hidden_bf16(4300 + M + K, M, K)
+        y = lin(dev_bf16(x)).cpu().numpy()
+        assert lin.device_error() == 0
+        y_o, A = oracle.gemv(oracle.FMT_NVFP4, q_o, sf_o, g_o, x)
+        check_logits(y, y_o, A, f"split linear K={K} M={M}")
+    if K == 5120:
+        wl = Workload(4400, 9000, K, 6100, 7, 4401)
+        headp, _ = gpu_nvfp4(wl, packed=True)
+        q_w, sf_w, g_w = wl.nvfp4()
+        for M in (7, 16):
+            run_step(headp, syn.hidden_bf16(4500 + M, M, K), oracle.FMT_NVFP4, q_w, sf_w, g_w, wl.idx, wl.n_kept,
+                     wl.V, f"split head M={M}")
+
+
+@pytest.mark.parametrize("fmt", ["nvfp4", "fp8", "w8a8", "bf16"])
+def test_k_split_formats(fmt):
+    """The canonical NVFP4, FP8 (W8A16 and W8A8) and BF16 heads at K = 5,120,
+    where every draft count splits K over a CTA pair (W8A8: the per-token
+    activation scale is the max over both halves), plus 16 drafts at K =
+    2,560 (one tile in flight; BF16 h fragments in shared memory). 376 tiles:
+    a pair takes more tiles than it has exchange slots."""
+    for K, Ms in ((5120, (1, 2, 4, 8, 16)), (2560, (16,))):
+        wl = Workload(4600 + K, 8000, K, 6000, 9, 4601 + K)
+        if fmt == "nvfp4":
+            head, _ = gpu_nvfp4(wl)
+            q_o, sf_o, g_o = wl.nvfp4()
+            ref = lambda h: oracle.gemv(oracle.FMT_NVFP4, q_o, sf_o, g_o, h)
+        elif fmt in ("fp8", "w8a8"):
+            head, (q, s) = gpu_fp8(wl)
+            q_o, s_o = wl.fp8()
+            if fmt == "w8a8":
+                head = dh.DraftHead(dh.DH_FMT_FP8_W8A8, wl.V, q, dev(wl.idx), wl.n_kept, scale=s, idx_ascending=True)
+
+                def ref(h):
+                    qx, sx = oracle.fp8_act_quantize(h)
+                    return oracle.gemv_w8a8(q_o, s_o, qx, sx)
+            else:
+                ref = lambda h: oracle.gemv(oracle.FMT_FP8, q_o, None, s_o, h)
+        else:
+            head = dh.bf16_full_head(dev_bf16(wl.W))
+            ref = lambda h: oracle.gemv(oracle.FMT_BF16, wl.W, None, None, h)
+        idx = None if fmt == "bf16" else wl.idx
+        n_kept = wl.V if fmt == "bf16" else wl.n_kept
+        for M in Ms:
+            h = syn.hidden_bf16(4700 + M + K, M, K)
+            y, A = ref(h)
+            check_step(head, h, y, A, idx, n_kept, wl.V, f"{fmt} K={K} M={M}")
+
+
 @pytest.mark.parametrize("n_rows,M", [(4096, 1), (4096, 5), (64, 2), (16_384, 16)])
 def test_tiny_bf16_truncated_head_step(tiny, n_rows, M):
     """The truncated BF16 draft head (the first n_rows ids of the target head):
