@@ -103,7 +103,8 @@ struct Cfg {
     // 80-register cap of two CTAs per SM spills.
     static constexpr bool TWO_CTA = FMT == kFmtPackedRing && MT <= 2 && NWIN == 20;
     // Register-load kernels with more windows than compute warps (K = 4,096
-    // and 5,120; the packed head at 8 and 16 drafts, fewer take the ring): the
+    // and 5,120; the packed head at 16 drafts, and at 8 for K = 5,120, whose
+    // two-window warps spill there; fewer drafts take the ring): the
     // K range is split over the two CTAs of a cluster, each with one window
     // per warp; the second CTA's reducer sends its sums into the first CTA's
     // shared memory (distributed shared memory), which writes the results.
@@ -111,7 +112,8 @@ struct Cfg {
     // 160 KB at K = 5,120 and 16 drafts) bounded these kernels, and no warp
     // holds two windows' h fragments (which spilled at 80 registers).
     static constexpr int KS =
-        (FMT != kFmtPackedRing && NWIN > kMaxComputeWarps && (FMT != kFmtPackedLdg || MT >= 8)) ? 2 : 1;
+        (FMT != kFmtPackedRing && NWIN > kMaxComputeWarps &&
+         (FMT != kFmtPackedLdg || MT >= 16 || (MT >= 8 && NWIN > 2 * 16))) ? 2 : 1;
     static constexpr int NWC = NWIN / KS;                    // windows of one CTA
     static constexpr int XS = 4;                             // exchange slots of a pair
     static constexpr int NW = largest_divisor_at_most(NWC, TWO_CTA ? 10 : kMaxComputeWarps);  // compute warps
@@ -141,7 +143,8 @@ struct Cfg {
     // µs per step. Slower at 2 drafts (+0.5 µs) and at 16 (+2.3 µs with two
     // tiles in flight; spills with three). Packed layout only: the canonical
     // layout's scale ring owns the dynamic shared memory.
-    static constexpr bool SMB = !BLOCKDIAG && ((PACKED && WPW == 1 && (MT == 4 || MT == 8)) || (FMT == 3 && MT >= 16));
+    static constexpr bool SMB = !BLOCKDIAG && ((PACKED && WPW == 1 && (MT == 4 || MT == 8)) || (FMT == 3 && MT >= 16) ||
+                                               (FMT == kFmtPackedRing && WPW == 2 && MT == 4 && NWIN > 32));
     // Register-load kernels: tiles of loads in flight in registers, as many as
     // fit next to the h fragments (16 registers per window and n8 tile) in the
     // 80 registers that 21+ warps per SM allow, up to a cap: three with one n8
@@ -151,7 +154,7 @@ struct Cfg {
     // packed NVFP4 head (9 registers a tile) two at one draft (20.00 -> 19.94
     // µs against three), four at two and eight drafts (21.43 -> 20.99, 22.19 ->
     // 21.55; four at four drafts was slower), two at 16 (three spilled).
-    static constexpr int PCAP = PACKED ? (MT == 1 ? 2 : (MT == 2 ? 4 : (MT >= 16 ? 2 : 3)))
+    static constexpr int PCAP = PACKED ? (MT == 1 ? 2 : (MT == 2 ? 4 : (MT >= 16 ? ((KS == 2 && NWIN > 32) ? 1 : 2) : 3)))
                                        : (MT >= 16 ? 1 : ((FMT == 2 || FMT == 5) ? 2 : 3));
     // Packed layout: the head streams through a ring of whole tiles in shared
     // memory, filled by one producer thread with 1-D bulk copies (the tiles of
@@ -201,10 +204,11 @@ struct Cfg {
     static constexpr int RT = RING ? cclamp((RING_BUDGET - PART_DYN - SMB_BYTES) / TB, 2, 8) : 0;
     static constexpr int NSB = RING ? RT : SS;                         // tile / scale ring barriers
     // K split: the exchange area after the scale ring or the h fragments:
-    // the sums' slots, their full and empty barriers, and (W8A8) the
-    // partner's max |h| per draft with its barrier
+    // the sums' slots, the first CTA's own sums and ids of the tile in hand,
+    // the slots' full and empty barriers, and (W8A8) the partner's max |h|
+    // per draft with its barrier
     static constexpr int XOFF = LOADER ? SS * SLOT : SMB_BYTES;
-    static constexpr int XB_BYTES = KS == 2 ? XS * 16 * MT * 4 + 2 * XS * 8 + 16 * 4 + 8 : 0;
+    static constexpr int XB_BYTES = KS == 2 ? (XS + 2) * 16 * MT * 4 + 2 * XS * 8 + 16 * 4 + 8 : 0;
     static constexpr size_t DYN_SMEM = RING ? static_cast<size_t>(RT) * TB + PART_DYN + SMB_BYTES
                                             : static_cast<size_t>(XOFF + XB_BYTES);
     static_assert(!(KS == 2 && RING), "the K split is for the register-load kernels");
@@ -255,6 +259,22 @@ struct TileBuf {
     uint2 s[C::WPW][2];
     uint32_t sp[C::WPW];
 };
+
+// Shared-memory reads that stay where they stand in program order (not
+// hoisted above the preceding math), so that a window's operands occupy
+// registers only while it is processed.
+__device__ __forceinline__ uint4 lds_v4_ordered(const void* p) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(smem_u32(p)) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ uint32_t lds_u32_ordered(const void* p) {
+    uint32_t v;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(smem_u32(p)) : "memory");
+    return v;
+}
 
 template <int FMT, int K, int MT>
 __device__ __forceinline__ void load_tile(TileBuf<FMT, K, MT>& b, const uint8_t* q, int tile, int wbase, int g,
@@ -336,7 +356,7 @@ __global__ void __launch_bounds__(Cfg<FMT, K, MT>::THREADS, Cfg<FMT, K, MT>::MIN
     // sums [slot][row][draft] in the first CTA, which waits on xfull[slot];
     // the second waits on xempty[slot] until the first has read a slot
     float* const s_xb = reinterpret_cast<float*>(s_dyn + C::XOFF);
-    uint64_t* const xfull = reinterpret_cast<uint64_t*>(s_dyn + C::XOFF + C::XS * NRED * 4);
+    uint64_t* const xfull = reinterpret_cast<uint64_t*>(s_dyn + C::XOFF + (C::XS + 2) * NRED * 4);
     uint64_t* const xempty = xfull + C::XS;
     float* const amx_rx = reinterpret_cast<float*>(xempty + C::XS);  // W8A8: the partner's max |h| per draft
     uint64_t* const amx_bar = reinterpret_cast<uint64_t*>(amx_rx + 16);
@@ -346,13 +366,11 @@ __global__ void __launch_bounds__(Cfg<FMT, K, MT>::THREADS, Cfg<FMT, K, MT>::MIN
     // tiles go to CTAs, or with the K split to pairs (clusters of two)
     const int crank = C::KS == 2 ? static_cast<int>(cluster_ctarank()) : 0;
     const int b0 = C::KS == 2 ? static_cast<int>(cluster_id_x()) : static_cast<int>(blockIdx.x);
-    // (read where used, not held in a register)
-    auto n_units = [&]() -> int {
-        if constexpr (C::KS == 2) return static_cast<int>(cluster_count_x());
-        else return static_cast<int>(gridDim.x);
-    };
-    const int my_tiles = b0 < n_tiles ? (n_tiles - 1 - b0) / n_units() + 1 : 0;
-    auto tile_of = [&](int i) { return b0 + i * n_units(); };
+    const int my_tiles = b0 < n_tiles
+                             ? (n_tiles - 1 - b0) / static_cast<int>(C::KS == 2 ? cluster_count_x() : gridDim.x) + 1
+                             : 0;
+    // (the unit count is read where used, not held in a register)
+    auto tile_of = [&](int i) { return b0 + i * static_cast<int>(C::KS == 2 ? cluster_count_x() : gridDim.x); };
     const int wbase = crank * C::NWC + warp;  // a compute warp's first window
     const bool xsend = C::KS == 2 && crank == 1;  // sends its sums instead of writing results
     const uint8_t* q = static_cast<const uint8_t*>(a.q);
@@ -506,7 +524,8 @@ __global__ void __launch_bounds__(Cfg<FMT, K, MT>::THREADS, Cfg<FMT, K, MT>::MIN
         constexpr int NU = 16 * UPR;                                     // units per tile
         constexpr int SLOTS = (NU + 32 * C::NRW - 1) / (32 * C::NRW);  // units per reducer thread
         static_assert(C::KS == 1 || NU <= 32 * C::NRW, "K split: at most one unit per reducer thread");
-        // the logit of (tile row row_t, draft m0 + d), written or kept as a key
+        // K split: the logit of (tile row row_t, draft m0 + d), written or kept
+        // as a key (the unsplit kernels do the same inline)
         auto emit = [&](int r0, int row_t, int m0, const float (&v)[DV], int id) {
             const int row = r0 + row_t;
             if (row >= a.n_kept) return;
@@ -535,23 +554,21 @@ __global__ void __launch_bounds__(Cfg<FMT, K, MT>::THREADS, Cfg<FMT, K, MT>::MIN
                 *abort_flag = 1;
             }
         };
-        // K split, first CTA: tile j's own sums wait in registers until the
-        // next tile's partials are in; then the partner's sums of tile j (in
-        // flight meanwhile) are added and the results written. Every reducer
-        // thread waits and arrives; those with a unit (rl < NU) also read and
-        // write.
-        float vprev[DV];
-#pragma unroll
-        for (int d = 0; d < DV; ++d) vprev[d] = 0.0f;
-        int idprev = 0, r0prev = 0;
+        // K split, first CTA: tile j's own sums wait (in this thread's place
+        // of the exchange area's own-sum row) until the next tile's partials
+        // are in; then the partner's sums of tile j (in flight meanwhile) are
+        // added and the results written. Every reducer thread waits and
+        // arrives; those with a unit (rl < NU) also read and write.
+        float* const s_own = s_xb + C::XS * NRED;  // [unit][d], then the units' ids
+        int* const s_ownid = reinterpret_cast<int*>(s_own + NRED);
         auto finish_prev = [&](int j) {
             const int xj = j % C::XS;
             xwait(&xfull[xj], (j / C::XS) & 1);
             if (rl < NU) {
                 float v[DV];
 #pragma unroll
-                for (int d = 0; d < DV; ++d) v[d] = vprev[d] + s_xb[xj * NRED + rl * DV + d];
-                emit(r0prev, rl / UPR, (rl % UPR) * DV, v, idprev);
+                for (int d = 0; d < DV; ++d) v[d] = s_own[rl * DV + d] + s_xb[xj * NRED + rl * DV + d];
+                emit(tile_of(j) * 16, rl / UPR, (rl % UPR) * DV, v, s_ownid[rl]);
             }
             if (j + C::XS < my_tiles) mbar_arrive_remote(cluster_map(&xempty[xj], 1));
         };
@@ -638,16 +655,33 @@ __global__ void __launch_bounds__(Cfg<FMT, K, MT>::THREADS, Cfg<FMT, K, MT>::MIN
                         else st_cluster_f32(ra, v[0]);
                     } else {
 #pragma unroll
-                        for (int d = 0; d < DV; ++d) vprev[d] = v[d];
-                        idprev = ids_[k];
+                        for (int d = 0; d < DV; ++d) s_own[u * DV + d] = v[d];
+                        s_ownid[u] = ids_[k];
                     }
                 } else {
-                    emit(r0, row_t, m0, v, ids_[k]);
+                    const int row = r0 + row_t;
+                    if (row >= a.n_kept) continue;
+#pragma unroll
+                    for (int d = 0; d < DV; ++d) {
+                        const int m = m0 + d;
+                        if (m >= a.M) break;
+                        if constexpr (LOGITS) {
+                            // an id outside [0, V) is reported, not written
+                            const int id = ids_[k];
+                            if (id >= 0 && id < a.V) a.out[static_cast<size_t>(m) * a.V + id] = v[d] * gmul;
+                            else atomicOr(&a.ws->error, kDevErrIdx);
+                        } else {
+                            // tie-break on the lower id (ascending dh_idx) or the lower row
+                            const unsigned long long key =
+                                argmax_key(ordered_key(v[d] * gmul), static_cast<uint32_t>(ids_[k]));
+                            const int r = row_t * MT + m;
+                            if (key > s_best[r]) s_best[r] = key;
+                        }
+                    }
                 }
             }
             if constexpr (C::KS == 2) {
                 if (xsend) mbar_arrive_remote(cluster_map(&xfull[xi], 0));
-                else r0prev = r0;
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty_p[slot]);
@@ -658,7 +692,11 @@ __global__ void __launch_bounds__(Cfg<FMT, K, MT>::THREADS, Cfg<FMT, K, MT>::MIN
         // K split: this thread's stores into the partner's shared memory and
         // arrivals on its barriers are complete before it passes the final
         // cluster barrier (the partner then exits)
-        if constexpr (C::KS == 2) cluster_fence();
+        // (the first CTA reaches into the second only for the slots it frees
+        // while more than XS tiles remain)
+        if constexpr (C::KS == 2) {
+            if (xsend || my_tiles > C::XS) cluster_fence();
+        }
     } else {
         // -------------------------------------------------- compute warps ----
         // This thread's h words (B fragments), per window and n8 tile: word j
@@ -859,7 +897,12 @@ __global__ void __launch_bounds__(Cfg<FMT, K, MT>::THREADS, Cfg<FMT, K, MT>::MIN
                 load_tile<FMT, K, MT>(b, q, tile_of(i), wbase, g, t);
             }
         };
-        if constexpr (C::RING) {
+        // Ring kernels with two windows per warp and n8 tiles of drafts: each
+        // window's codes and scales are read from the ring just before its
+        // math, not a tile ahead (one window's registers held instead of two:
+        // the two-window h fragments leave no room at 80 registers)
+        constexpr bool JIT = C::RING && WPW > 1 && !C::BLOCKDIAG;
+        if constexpr (C::RING && !JIT) {
 #pragma unroll
             for (int p = 0; p < P; ++p)
                 if (p < my_tiles) fetch(buf[p], p);
@@ -899,7 +942,8 @@ __global__ void __launch_bounds__(Cfg<FMT, K, MT>::THREADS, Cfg<FMT, K, MT>::MIN
                 if (ti >= my_tiles) break;
                 TileBuf<FMT, K, MT>& b = buf[p];
                 float out[NT][4];  // block-diagonal: out[0][0..1] = rows g, g+8
-
+                const int rs = ti % RTm;  // ring slot of this tile
+                if constexpr (JIT) pipe_wait(&full_s[rs], (ti / RTm) & 1);
 
                 if constexpr (C::SCALES) {
                     const int ss = ti % C::SS;
@@ -987,6 +1031,12 @@ __global__ void __launch_bounds__(Cfg<FMT, K, MT>::THREADS, Cfg<FMT, K, MT>::MIN
                     }
 #pragma unroll
                     for (int ww = 0; ww < (C::W8A8 ? 0 : WPW); ++ww) {
+                        if constexpr (JIT) {
+                            const uint8_t* blk = s_dyn + static_cast<size_t>(rs) * C::TB + (wbase + ww * NW) * C::WBLK;
+                            b.c[ww][0][0] = lds_v4_ordered(blk + g * 64 + 16 * t);
+                            b.c[ww][1][0] = lds_v4_ordered(blk + (g + 8) * 64 + 16 * t);
+                            b.sp[ww] = lds_u32_ordered(blk + 16 * 64 + 4 * lane);
+                        }
                         uint32_t sg0 = 0u, sg1 = 0u, sh0 = 0u, sh1 = 0u;  // (s, s) f16x2 per row and block
                         if constexpr (C::NV) {
                             // blocks 2t, 2t+1 of the window: bytes 2t, 2t+1 of its 8 scale bytes
@@ -1066,17 +1116,22 @@ __global__ void __launch_bounds__(Cfg<FMT, K, MT>::THREADS, Cfg<FMT, K, MT>::MIN
                         }
                     }
                 }
-                // loads of the tile P steps ahead go into the buffer just consumed
-                const int tn = ti + P;
-                if (tn < my_tiles) fetch(buf[p], tn);
+                if constexpr (JIT) {
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&empty_s[rs]);  // this warp is done with the slot
+                } else {
+                    // loads of the tile P steps ahead go into the buffer just consumed
+                    const int tn = ti + P;
+                    if (tn < my_tiles) fetch(buf[p], tn);
+                }
                 handoff(ti, out);
             }
         }
     }
     // with the K split, neither CTA of a pair exits while the other may still
     // reach into its shared memory
-    __syncwarp();
     if constexpr (C::KS == 2) {
+        __syncwarp();
         // compute warps: the wait of the arrival at the start (W8A8: made in the prologue)
         if (!C::W8A8 && warp < NW) cluster_wait();
         cluster_sync_all();
