@@ -86,6 +86,13 @@ __device__ __forceinline__ void e2m1x8_to_f16x2(uint32_t w, uint32_t (&o)[4]) {
         : "=r"(o[0]), "=r"(o[1]), "=r"(o[2]), "=r"(o[3]) : "r"(w));
 }
 
+// f16x2 product (exact for an E2M1 code times an E4M3 scale).
+__device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+
 // Two E4M3 bytes (low 16 bits of w) to f16x2, low byte -> low half. Exact.
 __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t w) {
     uint32_t r;

@@ -241,12 +241,6 @@ __device__ __forceinline__ void mma_e4m3(float (&d)[4], uint32_t a0, uint32_t a1
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-__device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
-    uint32_t r;
-    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
-    return r;
-}
-
 // Code bytes of one tile held by one thread: per window, CPR 16-byte pieces of
 // row g and of row g+8, and for NVFP4 the scale bytes: in the packed layout the
 // word with the scales of blocks 2t, 2t+1 of rows g and g+8 (loaded with the
