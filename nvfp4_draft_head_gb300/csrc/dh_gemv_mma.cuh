@@ -143,7 +143,8 @@ struct Cfg {
     // µs per step. Slower at 2 drafts (+0.5 µs) and at 16 (+2.3 µs with two
     // tiles in flight; spills with three). Packed layout only: the canonical
     // layout's scale ring owns the dynamic shared memory.
-    static constexpr bool SMB = !BLOCKDIAG && ((PACKED && WPW == 1 && (MT == 4 || MT == 8)) || (FMT == 3 && MT >= 16) ||
+    static constexpr bool SMB = !BLOCKDIAG && ((PACKED && WPW == 1 && (MT == 4 || MT == 8)) ||
+                                               ((FMT == 3 || FMT == 5) && MT >= 16) ||
                                                (FMT == kFmtPackedRing && WPW == 2 && MT == 4 && NWIN > 32));
     // Register-load kernels: tiles of loads in flight in registers, as many as
     // fit next to the h fragments (16 registers per window and n8 tile) in the
@@ -155,7 +156,7 @@ struct Cfg {
     // µs against three), four at two and eight drafts (21.43 -> 20.99, 22.19 ->
     // 21.55; four at four drafts was slower), two at 16 (three spilled).
     static constexpr int PCAP = PACKED ? (MT == 1 ? 2 : (MT == 2 ? 4 : (MT >= 16 ? ((KS == 2 && NWIN > 32) ? 1 : 2) : 3)))
-                                       : (MT >= 16 ? 1 : ((FMT == 2 || FMT == 5) ? 2 : 3));
+                                       : (MT >= 16 ? (W8A8 ? 2 : 1) : ((FMT == 2 || FMT == 5) ? 2 : 3));
     // Packed layout: the head streams through a ring of whole tiles in shared
     // memory, filled by one producer thread with 1-D bulk copies (the tiles of
     // this layout are contiguous). Its first RPRE tiles are issued before the
@@ -785,6 +786,16 @@ __global__ void __launch_bounds__(Cfg<FMT, K, MT>::THREADS, Cfg<FMT, K, MT>::MIN
         }
         uint2* s_hb = reinterpret_cast<uint2*>(s_dyn + (C::RING ? static_cast<size_t>(C::RT) * C::TB + C::PART_DYN : 0)) +
                       (C::SMB ? warp * WPW * NT * 8 * 32 : 0);  // [ww][nt][i][lane]
+        if constexpr (C::W8A8 && C::SMB) {
+            // the drafts' E4M3 codes (words 0..7 of hb) to shared memory
+#pragma unroll
+            for (int ww = 0; ww < WPW; ++ww)
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        s_hb[((ww * NT + nt) * 8 + i) * 32 + lane] = make_uint2(hb[ww][nt][2 * i], hb[ww][nt][2 * i + 1]);
+        }
 #pragma unroll
         for (int nt = 0; nt < (C::W8A8 ? 0 : NT); ++nt) {
             const int d = C::BLOCKDIAG ? 0 : g + 8 * nt;
@@ -1019,8 +1030,14 @@ __global__ void __launch_bounds__(Cfg<FMT, K, MT>::THREADS, Cfg<FMT, K, MT>::MIN
                                 const uint32_t a2 = word_of<C::CPR>(b.c[ww][0], 2 * i + 1);
                                 const uint32_t a3 = word_of<C::CPR>(b.c[ww][1], 2 * i + 1);
 #pragma unroll
-                                for (int nt = 0; nt < NT; ++nt)
-                                    mma_e4m3(out[nt], a0, a1, a2, a3, hb[ww][nt][2 * i], hb[ww][nt][2 * i + 1]);
+                                for (int nt = 0; nt < NT; ++nt) {
+                                    if constexpr (C::SMB) {
+                                        const uint2 bb = s_hb[((ww * NT + nt) * 8 + i) * 32 + lane];
+                                        mma_e4m3(out[nt], a0, a1, a2, a3, bb.x, bb.y);
+                                    } else {
+                                        mma_e4m3(out[nt], a0, a1, a2, a3, hb[ww][nt][2 * i], hb[ww][nt][2 * i + 1]);
+                                    }
+                                }
                             }
                     }
 #pragma unroll
