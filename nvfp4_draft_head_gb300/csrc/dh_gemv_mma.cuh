@@ -87,7 +87,8 @@ constexpr int kIdCap = 48;
 constexpr int kFmtPackedRing = 4;
 constexpr int kFmtPackedLdg = 6;
 
-template <int FMT, int K, int MT>
+// LG: the compute_logits variant (some choices depend on its extra register use)
+template <int FMT, int K, int MT, bool LG = false>
 struct Cfg {
     static constexpr int NWIN = K / 128;                     // 128-wide k-windows per row
     static constexpr bool PACKED = (FMT == kFmtPackedRing || FMT == kFmtPackedLdg);  // tile-major NVFP4 layout
@@ -99,9 +100,12 @@ struct Cfg {
     // retires, a CTA of the next launch takes its place and starts streaming
     // while the other finishes, and each warp's per-tile hand-off and shuffles
     // cover two windows. Measured (one draft, 1,000 graph steps): 18.0 -> 17.0
-    // µs top tokens, 19.8 -> 18.4 compute_logits; at 4 drafts and more the
-    // 80-register cap of two CTAs per SM spills.
-    static constexpr bool TWO_CTA = FMT == kFmtPackedRing && MT <= 2 && NWIN == 20;
+    // µs top tokens, 19.8 -> 18.4 compute_logits; four drafts with one reducer
+    // warp and each window read from the ring just before its math: 20.5 ->
+    // 19.8 top tokens, 22.1 -> 21.6 compute_logits (with shared-memory h
+    // fragments, which its registers need). At 8 drafts the 80-register cap
+    // of two CTAs per SM spills.
+    static constexpr bool TWO_CTA = FMT == kFmtPackedRing && MT <= 4 && NWIN == 20;
     // Register-load kernels with more windows than compute warps (K = 4,096
     // and 5,120; the packed head at 16 drafts, and at 8 for K = 5,120, whose
     // two-window warps spill there; fewer drafts take the ring): the
@@ -145,7 +149,7 @@ struct Cfg {
     // layout's scale ring owns the dynamic shared memory.
     static constexpr bool SMB = !BLOCKDIAG && ((PACKED && WPW == 1 && (MT == 4 || MT == 8)) ||
                                                ((FMT == 3 || FMT == 5) && MT >= 16) ||
-                                               (FMT == kFmtPackedRing && WPW == 2 && MT == 4 && NWIN > 32));
+                                               (FMT == kFmtPackedRing && WPW == 2 && MT == 4 && (NWIN > 32 || LG)));
     // Register-load kernels: tiles of loads in flight in registers, as many as
     // fit next to the h fragments (16 registers per window and n8 tile) in the
     // 80 registers that 21+ warps per SM allow, up to a cap: three with one n8
@@ -184,7 +188,7 @@ struct Cfg {
     // as a tree (one draft 21.3 -> 19.7 µs against the warp-major layout with
     // a sequential sum, where the single reducer warp fell behind).
     static constexpr bool RED_T = BLOCKDIAG;
-    static constexpr int NRW = MT >= 16 ? (16 * MT / DV) / 32 : (MT >= 8 ? 4 : (MT >= 4 ? 2 : 1));  // reducer warps
+    static constexpr int NRW = TWO_CTA ? 1 : (MT >= 16 ? (16 * MT / DV) / 32 : (MT >= 8 ? 4 : (MT >= 4 ? 2 : 1)));  // reducer warps
     static constexpr int THREADS = (NW + NRW + ((LOADER || RING) ? 1 : 0)) * 32;  // + reducers (+ loader / producer)
     static constexpr int SLOT = 16 * SFB;                              // bytes of one ring slot
     static constexpr int SS = 6;
@@ -318,8 +322,9 @@ __device__ __forceinline__ uint32_t word_of(const uint4 (&v)[CPR], int i) {
 }
 
 template <int FMT, int K, int MT, bool LOGITS>
-__global__ void __launch_bounds__(Cfg<FMT, K, MT>::THREADS, Cfg<FMT, K, MT>::MINB) gemv_mma_kernel(const GemvArgs a) {
-    using C = Cfg<FMT, K, MT>;
+__global__ void __launch_bounds__(Cfg<FMT, K, MT, LOGITS>::THREADS, Cfg<FMT, K, MT, LOGITS>::MINB)
+    gemv_mma_kernel(const GemvArgs a) {
+    using C = Cfg<FMT, K, MT, LOGITS>;
     constexpr int NW = C::NW, WPW = C::WPW, NT = C::NT, P = C::P, KW = K / 2, RS = C::RS;
     constexpr int NRED = 16 * MT;  // (row, draft) results of a tile
     constexpr int RTm = C::RT > 0 ? C::RT : 1;
@@ -1165,7 +1170,7 @@ __global__ void __launch_bounds__(Cfg<FMT, K, MT>::THREADS, Cfg<FMT, K, MT>::MIN
 
 template <int FMT, int K, int MT, bool LOGITS>
 inline cudaError_t launch_mma(const GemvArgs& a, cudaStream_t s) {
-    using C = Cfg<FMT, K, MT>;
+    using C = Cfg<FMT, K, MT, LOGITS>;
     auto kern = gemv_mma_kernel<FMT, K, MT, LOGITS>;
     const int sms = sm_count();
     if (sms <= 0) return cudaErrorInvalidDevice;
