@@ -101,11 +101,11 @@ struct Cfg {
     // while the other finishes, and each warp's per-tile hand-off and shuffles
     // cover two windows. Measured (one draft, 1,000 graph steps): 18.0 -> 17.0
     // µs top tokens, 19.8 -> 18.4 compute_logits; four drafts with one reducer
-    // warp and each window read from the ring just before its math: 20.5 ->
-    // 19.8 top tokens, 22.1 -> 21.6 compute_logits (with shared-memory h
-    // fragments, which its registers need). At 8 drafts the 80-register cap
-    // of two CTAs per SM spills.
-    static constexpr bool TWO_CTA = FMT == kFmtPackedRing && MT <= 4 && NWIN == 20;
+    // warp (two drafts per unit) and each window read from the ring just
+    // before its math: 20.5 -> 19.7 top tokens, 22.1 -> 21.4 compute_logits
+    // (with shared-memory h fragments, which its registers need); eight
+    // drafts, compute_logits only: 23.3 -> 22.4 (top tokens 21.6 -> 22.9).
+    static constexpr bool TWO_CTA = FMT == kFmtPackedRing && MT <= 8 && NWIN == 20;
     // Register-load kernels with more windows than compute warps (K = 4,096
     // and 5,120; the packed head at 16 drafts, and at 8 for K = 5,120, whose
     // two-window warps spill there; fewer drafts take the ring): the
@@ -149,7 +149,8 @@ struct Cfg {
     // layout's scale ring owns the dynamic shared memory.
     static constexpr bool SMB = !BLOCKDIAG && ((PACKED && WPW == 1 && (MT == 4 || MT == 8)) ||
                                                ((FMT == 3 || FMT == 5) && MT >= 16) ||
-                                               (FMT == kFmtPackedRing && WPW == 2 && MT == 4 && (NWIN > 32 || LG)));
+                                               (FMT == kFmtPackedRing && WPW == 2 &&
+                                                ((MT == 4 && (NWIN > 32 || LG)) || (MT == 8 && LG))));
     // Register-load kernels: tiles of loads in flight in registers, as many as
     // fit next to the h fragments (16 registers per window and n8 tile) in the
     // 80 registers that 21+ warps per SM allow, up to a cap: three with one n8
@@ -182,7 +183,7 @@ struct Cfg {
     static constexpr bool SCALES = (FMT == 1);
     static constexpr bool LOADER = SCALES;
     // reducer unit: one row and DV drafts (one float2 read per partial at 16 drafts)
-    static constexpr int DV = MT >= 16 ? 2 : 1;
+    static constexpr int DV = (MT >= 16 || (TWO_CTA && MT >= 4)) ? 2 : 1;
     // One draft: the partial sums are stored row-major ([slot][row][warp]), so
     // a reducer lane reads its row's partials with 16-byte loads and sums them
     // as a tree (one draft 21.3 -> 19.7 µs against the warp-major layout with
@@ -1254,6 +1255,9 @@ inline cudaError_t launch_ring_k(const GemvArgs& a, cudaStream_t s) {
     if (a.out) {
         if (a.M <= 1) return launch_mma<kFmtPackedRing, K, 1, true>(a, s);
         if (a.M <= 2) return launch_mma<kFmtPackedRing, K, 2, true>(a, s);
+        if constexpr (K == 2560) {
+            if (a.M > 4) return launch_mma<kFmtPackedRing, K, 8, true>(a, s);  // compute_logits only
+        }
         return launch_mma<kFmtPackedRing, K, 4, true>(a, s);
     }
     if (a.M <= 1) return launch_mma<kFmtPackedRing, K, 1, false>(a, s);
@@ -1261,13 +1265,15 @@ inline cudaError_t launch_ring_k(const GemvArgs& a, cudaStream_t s) {
     return launch_mma<kFmtPackedRing, K, 4, false>(a, s);
 }
 
-// Packed head: the ring kernel for up to four drafts, K >= 2560, on heads of at
-// least eight tiles per SM or K >= 4096 (one draft, 64,064 x 2560: 19.8 ->
-// 16.9 µs; 4 drafts 21.4 -> 20.4); register loads otherwise (8 and 16 drafts,
-// where the ring measured 0.8 and 2.5 µs slower; the 4,032 x 256 head; the
-// 1,024 - 4,608-row linears at K <= 2560).
+// Packed head: the ring kernel for up to four drafts (eight for compute_logits
+// at K = 2560), K >= 2560, on heads of at least eight tiles per SM or K >= 4096
+// (one draft, 64,064 x 2560: 19.8 -> 16.9 µs; 4 drafts 21.4 -> 20.4); register
+// loads otherwise (top tokens at 8 drafts and 16 drafts, where the ring
+// measured 1.2 and 2.5 µs slower; the 4,032 x 256 head; the 1,024 - 4,608-row
+// linears at K <= 2560).
 inline bool packed_use_ring(const GemvArgs& a) {
-    return a.M <= 4 && a.K >= 2560 && (a.N / 16 >= 8 * sm_count() || a.K >= 4096);
+    return (a.M <= 4 || (a.M <= 8 && a.K == 2560 && a.out != nullptr)) && a.K >= 2560 &&
+           (a.N / 16 >= 8 * sm_count() || a.K >= 4096);
 }
 
 }  // namespace mma
