@@ -205,8 +205,10 @@ struct Cfg {
     static constexpr int SMB_BYTES = SMB ? NW * WPW * NT * 8 * 32 * 8 : 0;
     // packed layout: dynamic shared memory of a CTA (one or two per SM) and
     // the tiles of its ring, as many as fit next to the partials and the h
-    // fragments, 2 to 8
-    static constexpr int RING_BUDGET = TWO_CTA ? 96 * 1024 : 200 * 1024;
+    // fragments, 2 to 8. Two CTAs per SM: three tiles at one draft, four at
+    // two and four drafts where the h fragments stay in registers (two drafts
+    // 18.64 -> 18.52 µs, four 19.71 -> 19.55; one draft 16.76 -> 16.90 with four)
+    static constexpr int RING_BUDGET = TWO_CTA ? (MT == 1 ? 96 : 104) * 1024 : 200 * 1024;
     static constexpr int RT = RING ? cclamp((RING_BUDGET - PART_DYN - SMB_BYTES) / TB, 2, 8) : 0;
     static constexpr int NSB = RING ? RT : SS;                         // tile / scale ring barriers
     // K split: the exchange area after the scale ring or the h fragments:
