@@ -51,9 +51,13 @@ cudaError_t launch_keys_to_ids(const unsigned long long* keys, int M, int32_t* i
 // Hidden rows from page-locked host memory into the workspace staging area,
 // 16 bytes per thread (a draft step's rows: M x K x 2 <= 16 x 5120 x 2 bytes).
 // The loads are issued before the grid-dependency wait (the host wrote the
-// rows before the call), the stores after it.
+// rows before the call), the stores after it. The draft step launched next
+// may start at once (it reads the staging area only after this grid has
+// completed): end to end 18.86 -> 18.27 µs a step against a release after
+// the stores.
 __global__ void __launch_bounds__(1024) stage_rows_kernel(const uint4* src, uint4* dst, int n16) {
     constexpr int kPer = 10;  // 16-byte pieces per thread: 1024 x 10 x 16 = 160 KB
+    asm volatile("griddepcontrol.launch_dependents;");
     uint4 v[kPer];
 #pragma unroll
     for (int j = 0; j < kPer; ++j) {
@@ -66,8 +70,6 @@ __global__ void __launch_bounds__(1024) stage_rows_kernel(const uint4* src, uint
         const int i = threadIdx.x + j * blockDim.x;
         if (i < n16) dst[i] = v[j];
     }
-    __syncthreads();
-    asm volatile("griddepcontrol.launch_dependents;");
 }
 
 cudaError_t launch_stage_rows(const void* src_host, void* dst, size_t bytes, cudaStream_t s) {
