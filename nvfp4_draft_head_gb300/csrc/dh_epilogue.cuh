@@ -44,13 +44,32 @@ __device__ __forceinline__ void finish_argmax(const GemvArgs& a, const unsigned 
     if (threadIdx.x == 0) s_late = 0;
     __syncthreads();
     const int G = static_cast<int>(gridDim.x);
-    for (int j = threadIdx.x; j < G * a.M; j += blockDim.x) {
-        const int m = j / G, b = j - m * G;
-        unsigned long long* p = &a.ws->slots[bank][m][b];
-        const unsigned long long v = poll_nonzero(p);
-        if (v == 0ull) s_late = 1;
-        asm volatile("st.relaxed.gpu.global.u64 [%0], 0;" :: "l"(p) : "memory");
-        if (v > 1ull) atomicMax(&s_red[m], v);
+    const int total = G * a.M;
+    // A thread reads up to four slots before it waits on any, so that with
+    // more slots than threads (several drafts) the keys that are already
+    // there cost one round trip, not one per slot.
+    for (int j0 = threadIdx.x; j0 < total; j0 += 4 * static_cast<int>(blockDim.x)) {
+        unsigned long long v[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int j = j0 + u * static_cast<int>(blockDim.x);
+            v[u] = 0ull;
+            if (j < total) {
+                const int m = j / G, b = j - m * G;
+                asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v[u]) : "l"(&a.ws->slots[bank][m][b]) : "memory");
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int j = j0 + u * static_cast<int>(blockDim.x);
+            if (j >= total) break;
+            const int m = j / G, b = j - m * G;
+            unsigned long long* p = &a.ws->slots[bank][m][b];
+            if (v[u] == 0ull) v[u] = poll_nonzero(p);
+            if (v[u] == 0ull) s_late = 1;
+            asm volatile("st.relaxed.gpu.global.u64 [%0], 0;" :: "l"(p) : "memory");
+            if (v[u] > 1ull) atomicMax(&s_red[m], v[u]);
+        }
     }
     // a dirty bank left by an earlier step (never this step's bank): zero the
     // slots that step used
