@@ -122,6 +122,35 @@ def test_batch_sweep_with_near_ties(qwen64k, head64k, M):
     assert planted_total >= 1
 
 
+@pytest.mark.parametrize("M", [1, 4, 16])
+def test_back_to_back_compute_logits_into_one_buffer(qwen64k, head64k, M):
+    """Consecutive compute_logits steps write one output buffer; each step's
+    -inf fill starts while the step before it finishes and must not write
+    before it has completed. Six steps with different hidden states, eager
+    and as one CUDA graph, end bitwise equal to a single step on the last."""
+    hs = [dev_bf16(syn.hidden_bf16(syn.hidden_seed(4, 100 * M + i), M, qwen64k.K)) for i in range(6)]
+    want = head64k.compute_logits(hs[-1])
+    out = torch.empty((M, qwen64k.V), dtype=torch.float32, device="cuda")
+    for h in hs:
+        head64k.compute_logits(h, out=out)
+    assert torch.equal(out.view(torch.int32), want.view(torch.int32))
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        head64k.compute_logits(hs[0], out=out)            # warm-up outside capture
+    torch.cuda.current_stream().wait_stream(s)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for h in hs:
+            head64k.compute_logits(h, out=out)
+    for _ in range(2):
+        out.zero_()
+        graph.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out.view(torch.int32), want.view(torch.int32))
+    assert head64k.device_error() == 0
+
+
 def test_fp8_98k_head(W_full, W_dev):
     c = syn.FP8_98K
     wl = Workload(syn.SEED_HEAD_QWEN, c["V"], c["K"], c["n_kept"], c["forced"], syn.SEED_KEEP_98K, W=W_full)

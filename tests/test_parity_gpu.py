@@ -548,6 +548,42 @@ def test_bounded_waits_give_up_and_report(tiny, kind):
     run_step(head, h, oracle.FMT_NVFP4, q_o, sf_o, g_o, tiny.idx, tiny.n_kept, tiny.V, f"after probe {kind}")
 
 
+@pytest.mark.parametrize("M", [1, 3, 16])
+def test_tiny_back_to_back_compute_logits(tiny, M):
+    """Consecutive compute_logits steps into one output buffer (each step's
+    -inf fill starts early and must wait for the step before it), eager and
+    as one CUDA graph: the buffer ends bitwise equal to one step on the last
+    hidden state, which meets the oracle's tolerance."""
+    head, _ = gpu_nvfp4(tiny, packed=True)
+    hb = [syn.hidden_bf16(syn.hidden_seed(0, 9200 + 10 * M + i), M, tiny.K) for i in range(6)]
+    hs = [dev_bf16(x) for x in hb]
+    want = head.compute_logits(hs[-1])
+    y_o, A = oracle.gemv(oracle.FMT_NVFP4, *tiny.nvfp4(), hb[-1])
+    kept = tiny.idx[: tiny.n_kept]
+    got = want.cpu().numpy()
+    check_logits(got[:, kept], y_o[:, : tiny.n_kept], A[:, : tiny.n_kept], f"back to back M={M}")
+    assert np.isneginf(np.delete(got, kept, axis=1)).all()
+    out = torch.empty((M, tiny.V), dtype=torch.float32, device="cuda")
+    for h in hs:
+        head.compute_logits(h, out=out)
+    assert torch.equal(out.view(torch.int32), want.view(torch.int32))
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        head.compute_logits(hs[0], out=out)               # warm-up outside capture
+    torch.cuda.current_stream().wait_stream(s)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for h in hs:
+            head.compute_logits(h, out=out)
+    for _ in range(2):
+        out.zero_()
+        graph.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out.view(torch.int32), want.view(torch.int32))
+    assert head.device_error() == 0
+
+
 @pytest.mark.parametrize("path", ["nvfp4_logits", "w8a8_top", "w8a8_logits", "linear"])
 def test_cuda_graph_replay_other_paths(tiny, path):
     """compute_logits (fill kernel + GEMV), the W8A8 step and the MTP-block linear
