@@ -242,8 +242,11 @@ int draft_head_top_tokens_host(const dh_head_t *hd, const void *h_host, int M, i
 /* compute_logits ("q38_draft.py" compute_logits; "FP8 MTP draft stack ...",
  * Qwen3_5MTP.compute_logits): out fp32 [M][V] row-major, 16-byte aligned;
  * out[m, :] = -inf, then out[m, idx[n]] = y[m, n] for n < n_kept. idx entries
- * of the kept rows must be distinct. Two kernel launches (the -inf fill, then
- * the GEMV writing its logits in place); capturable in a CUDA graph. */
+ * of the kept rows must be distinct. Two kernel launches, both with
+ * programmatic stream serialisation: the -inf fill, which writes out only
+ * after the kernel before it on the stream has completed, then the GEMV,
+ * which writes its logits in place once the fill has completed; capturable
+ * in a CUDA graph. */
 int draft_head_compute_logits(const dh_head_t *hd, const void *h, int M, float *out,
                               void *ws, size_t ws_bytes, void *stream);
 
